@@ -1,0 +1,24 @@
+"""GB300-native exact FlashAttention-2 forward (sm_103a, tcgen05 + TMA).
+
+The compute path is the C-ABI library ``libfa2_gb300.so`` built from
+``csrc/`` (declared in ``include/fa2.h``); this package is the thin Python
+binding over it.  The binding symbols (``fa2_fwd`` and friends) are resolved
+on first use: if the CUDA library has not been built, that raises ImportError
+-- there is no CPU fallback.
+
+``workloads`` (seeded synthetic inputs) imports no CUDA code and is usable on
+a machine without a GPU.
+"""
+from . import workloads  # noqa: F401
+
+_BINDING_NAMES = (
+    "fa2_fwd", "fa2_fwd_from_host", "fa2_get_device_error", "fa2_status_string",
+    "fa2_version", "Fa2Error", "library_path", "load_library", "STATUS",
+)
+
+
+def __getattr__(name):
+    if name in _BINDING_NAMES:
+        from . import _binding
+        return getattr(_binding, name)
+    raise AttributeError(name)

@@ -1,0 +1,130 @@
+"""fp64 CPU oracle for exact scaled-dot-product attention (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm are the only callers.  The CUDA
+library never imports, links or calls anything here, and this package imports
+nothing from the CUDA side.
+
+The arithmetic lives in ``fa2_oracle.c`` (plain C, fp64, one materialised score
+row and probability row per output row); this module only compiles it with gcc
+and marshals arguments.  See that file's header for the definition it follows:
+
+  O = softmax(scale * Q K^T [+ causal mask]) V,   LSE_i = ln sum_j exp(s_ij)
+
+as stated in Olowookere, "FlashAttention-2 from scratch with a custom Triton
+kernel" (section "The core idea: making attention IO-aware") and "Chapter 08:
+Flash Attention -- blocked attention" (sections 3 and 4).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms,
+invariants, brute force, a library cross-check); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa2_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libfa2_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, -O2, no fast-math). Returns the .so path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.fa2_oracle_rows.restype = ctypes.c_int
+            lib.fa2_oracle_rows.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int64, ctypes.c_int, ctypes.c_double,
+                ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.fa2_oracle_decode_bf16.restype = None
+            lib.fa2_oracle_decode_bf16.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+            lib.fa2_oracle_max_threads.restype = ctypes.c_int
+            lib.fa2_oracle_max_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _bf16_bits(t) -> np.ndarray:
+    """bf16 torch tensor (CPU) -> contiguous uint16 numpy array of its bits."""
+    import torch
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"oracle inputs must be bfloat16, got {t.dtype}")
+    t = t.detach().to("cpu").contiguous()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def decode_bf16(bits: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to fp64 the way the oracle does internally."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().fa2_oracle_decode_bf16(bits.ctypes.data, out.ctypes.data, bits.size)
+    return out
+
+
+def max_threads() -> int:
+    return int(_load().fa2_oracle_max_threads())
+
+
+def attention_rows(q, k, v, causal: bool, scale: float, rows=None,
+                   return_p: bool = False, threads: int = 0):
+    """Oracle output for selected rows.
+
+    q: bf16 (B, H, Lq, D); k, v: bf16 (B, H, Lk, D) (torch CPU or CUDA tensors).
+    rows: int64 array of flat row ids (b*H + h)*Lq + i; None means every row.
+    Returns (o (n, D) fp64, lse (n,) fp64[, p (n, Lk) fp64]).
+    """
+    B, H, Lq, D = q.shape
+    Bk, Hk, Lk, Dk = k.shape
+    if (Bk, Hk, Dk) != (B, H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q, k, v shapes disagree")
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    if rows is None:
+        rows = np.arange(B * H * Lq, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    o = np.empty((n, D), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    p = np.empty((n, Lk), dtype=np.float64) if return_p else None
+    rc = _load().fa2_oracle_rows(
+        qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
+        B, H, Lq, Lk, D, int(bool(causal)), float(scale),
+        rows.ctypes.data if n else None, n,
+        o.ctypes.data, lse.ctypes.data, p.ctypes.data if return_p else None,
+        int(threads))
+    if rc != 0:
+        raise RuntimeError(f"fa2_oracle_rows failed with code {rc}")
+    return (o, lse, p) if return_p else (o, lse)
+
+
+def attention(q, k, v, causal: bool, scale: float, threads: int = 0):
+    """Full oracle output: O fp64 (B, H, Lq, D) and LSE fp64 (B, H, Lq)."""
+    B, H, Lq, D = q.shape
+    o, lse = attention_rows(q, k, v, causal, scale, None, False, threads)
+    return o.reshape(B, H, Lq, D), lse.reshape(B, H, Lq)

@@ -1,0 +1,196 @@
+/*
+ * fa2_oracle.c -- plain, slow, fp64 CPU oracle for exact scaled-dot-product
+ * attention with per-row logsumexp.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference arm may load or call this code.  The
+ * product path (the CUDA library) never routes through it and shares no code,
+ * header, table or helper with it.
+ *
+ * What it computes (the textbook definition the FlashAttention pages state and
+ * that the tiled method reproduces exactly, up to rounding):
+ *
+ *   - Olowookere, "FlashAttention-2 from scratch with a custom Triton kernel",
+ *     section "The core idea: making attention IO-aware":
+ *         S = Q K^T,  P = softmax(S) (row-wise),  O = P V.
+ *   - "Flash Attention: principles and implementation" (tbr8.org), section 1
+ *     ("the compute bottleneck of attention"): softmax(Q K^T / sqrt(d)) V,
+ *     i.e. the scores carry the scale factor before the softmax.
+ *   - "Chapter 08: Flash Attention -- blocked attention" (chuoer47), section 3
+ *     ("LSE"): the per-row log-sum-exp LSE = m + log(l) is what a backward
+ *     pass needs; section 4 ("causal mask"): query i may see key j only when
+ *     j <= i (lower triangle including the diagonal).
+ *
+ * Readings taken where the pages are loose (each listed in the design doc):
+ *   - LSE is the NATURAL log of sum_j exp(s_ij) over the SCALED scores
+ *     s_ij = scale * q_i . k_j (the plain definition; page 4's base-2 value is
+ *     this times log2(e)).
+ *   - Masked positions are excluded exactly (weight 0), not given -1e6.
+ *   - Causal with Lq != Lk uses the literal top-left rule j <= i.
+ *   - Keys j >= Lk do not exist (no zero-padded keys take part).
+ *
+ * Per output row (b, h, i) the oracle MATERIALISES the full score row
+ * S[i, 0..Lk) and the full probability row P[i, 0..Lk) in fp64 before any
+ * reduction; there is no tiling, no online softmax, no fusion.
+ *
+ * Inputs are bf16 bit patterns (uint16) in contiguous (B, H, L, D) order; each
+ * is widened exactly to fp64 (bf16 is the top half of an IEEE binary32).
+ * Parallelism is over independent output rows only (OpenMP), which does not
+ * change any row's arithmetic.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 -> fp64, exact: the 16 bits are the high half of a binary32. */
+static double bf16_to_f64(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Exposed so a test can pin the widening against an independent decoder. */
+void fa2_oracle_decode_bf16(const uint16_t *src, double *dst, int64_t n)
+{
+    for (int64_t t = 0; t < n; ++t)
+        dst[t] = bf16_to_f64(src[t]);
+}
+
+/* Key j is visible to query i (causal mask of chapter 08, section 4). */
+static int allowed(int64_t i, int64_t j, int causal)
+{
+    return !causal || j <= i;
+}
+
+/*
+ * One output row.  s and p are caller-provided scratch rows of length Lk.
+ * Returns the number of visible keys |A_i|.
+ */
+static int64_t one_row(const uint16_t *q_row, const uint16_t *k_head,
+                       const uint16_t *v_head, int64_t i, int64_t Lk,
+                       int64_t D, int causal, double scale, double *s,
+                       double *p, double *o_row, double *lse_out)
+{
+    /* S row: s_j = scale * sum_d q_id k_jd  (fp64, inputs widened exactly). */
+    int64_t n_allowed = 0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (!allowed(i, j, causal)) {
+            s[j] = -INFINITY; /* not in A_i; never read below */
+            continue;
+        }
+        const uint16_t *k_row = k_head + j * D;
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            dot += bf16_to_f64(q_row[d]) * bf16_to_f64(k_row[d]);
+        s[j] = scale * dot;
+        if (s[j] > m)
+            m = s[j];
+        ++n_allowed;
+    }
+
+    /* P row: p_j = exp(s_j - M) / sum_{A_i} exp(s_j - M);  p_j = 0 off A_i. */
+    double z = 0.0;
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (allowed(i, j, causal)) {
+            p[j] = exp(s[j] - m);
+            z += p[j];
+        } else {
+            p[j] = 0.0;
+        }
+    }
+    for (int64_t j = 0; j < Lk; ++j)
+        p[j] = p[j] / z;
+
+    /* O row: o_d = sum_j p_j v_jd. */
+    for (int64_t d = 0; d < D; ++d)
+        o_row[d] = 0.0;
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (!allowed(i, j, causal))
+            continue;
+        const uint16_t *v_row = v_head + j * D;
+        for (int64_t d = 0; d < D; ++d)
+            o_row[d] += p[j] * bf16_to_f64(v_row[d]);
+    }
+
+    /* LSE_i = M + ln sum_{A_i} exp(s_j - M)  (= ln sum exp(s_j)). */
+    *lse_out = m + log(z);
+    return n_allowed;
+}
+
+/*
+ * Attention for a list of output rows.
+ *
+ *   q: bf16 bits (B, H, Lq, D);  k, v: bf16 bits (B, H, Lk, D); contiguous.
+ *   rows[r] = (b * H + h) * Lq + i selects output row r.
+ *   o:   fp64 (n_rows, D), lse: fp64 (n_rows).
+ *   p_out: optional fp64 (n_rows, Lk) copy of the materialised P rows.
+ *   n_threads <= 0 lets OpenMP choose.
+ *
+ * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
+ */
+int fa2_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t D,
+                    int causal, double scale, const int64_t *rows,
+                    int64_t n_rows, double *o, double *lse, double *p_out,
+                    int n_threads)
+{
+    if (!q || !k || !v || !o || !lse || (n_rows > 0 && !rows))
+        return 1;
+    if (B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0 || n_rows < 0)
+        return 1;
+    for (int64_t r = 0; r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= B * H * Lq)
+            return 1;
+
+    int failed = 0;
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)Lk * sizeof(double));
+        double *p = (double *)malloc((size_t)Lk * sizeof(double));
+        if (!s || !p) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t r = 0; r < n_rows; ++r) {
+                int64_t bh = rows[r] / Lq;
+                int64_t i = rows[r] % Lq;
+                const uint16_t *q_row = q + (bh * Lq + i) * D;
+                const uint16_t *k_head = k + bh * Lk * D;
+                const uint16_t *v_head = v + bh * Lk * D;
+                one_row(q_row, k_head, v_head, i, Lk, D, causal, scale, s, p,
+                        o + r * D, lse + r);
+                if (p_out)
+                    memcpy(p_out + r * Lk, p, (size_t)Lk * sizeof(double));
+            }
+        }
+        free(s);
+        free(p);
+    }
+    return failed ? 2 : 0;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int fa2_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
