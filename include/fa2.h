@@ -1,0 +1,117 @@
+/*
+ * fa2.h -- C ABI of the GB300 (sm_103a) exact FlashAttention-2 forward pass.
+ *
+ * The operation (one call = one forward pass over a batch of heads):
+ *
+ *     for every batch b < B, head h < H, query row i < Lq:
+ *         s_ij   = scale * sum_d Q[b,h,i,d] * K[b,h,j,d]      for visible keys j
+ *         O[b,h,i,:] = sum_j softmax_j(s_i.) * V[b,h,j,:]
+ *         LSE[b,h,i] = ln sum_j exp(s_ij)                       (natural log)
+ *
+ * with visible keys j < Lk, and additionally j <= i when causal != 0.
+ * This is exact scaled-dot-product attention as defined in Olowookere,
+ * "FlashAttention-2 from scratch with a custom Triton kernel" (section "The
+ * core idea: making attention IO-aware": S = QK^T, P = softmax(S), O = PV,
+ * computed by streaming K/V blocks with an online softmax and never writing
+ * the score matrix to memory), with the causal rule and the per-row
+ * log-sum-exp output of "Chapter 08: Flash Attention -- blocked attention"
+ * (sections 3 "LSE" and 4 "causal mask"), and the host-wrapper contract of
+ * page 1's section "Host wrapper and kernel launch" (inputs in, O and the
+ * per-row statistic out, grid over query blocks x batch*head).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are dense, row-major, contiguous:
+ *       q, o : bf16 [B, H, Lq, D]      k, v : bf16 [B, H, Lk, D]
+ *       lse  : fp32 [B, H, Lq]
+ *     bf16 is passed as raw 16-bit storage (void*).
+ *   - D must be 64, 128 or 256.  scale must be finite and > 0 (the pages use
+ *     1/sqrt(D)).  Causal with Lq != Lk uses the top-left rule j <= i.
+ *   - Device pointers must be 16-byte aligned (TMA requirement); lse 4-byte.
+ *   - The caller owns every buffer.  No entry point allocates device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are stream-ordered and asynchronous: they return once
+ *     the work is enqueued, and never synchronise except where stated.
+ *   - Re-entrant and thread-safe; the library keeps no per-call state.
+ *   - O and LSE rows i >= Lq are never written; inputs are never written.
+ */
+#ifndef FA2_GB300_H
+#define FA2_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa2_status {
+    FA2_OK = 0,
+    FA2_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad scale */
+    FA2_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (D) */
+    FA2_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    FA2_ERR_TIMEOUT = 4       /* a kernel wait exceeded its limit (see below) */
+} fa2_status;
+
+/*
+ * fa2_fwd -- the forward pass on device buffers.
+ *
+ *   q, k, v  device pointers to the bf16 inputs (read only).
+ *   o        device pointer, bf16 [B, H, Lq, D] output.
+ *   lse      device pointer, fp32 [B, H, Lq] output, natural-log LSE.
+ *   B, H     batch and head counts (>= 1, B*H <= 2^31 - 1).
+ *   Lq, Lk   query / key lengths (Lq >= 0, Lk >= 1).  Lq == 0 is a no-op.
+ *   D        head dimension: 64, 128 or 256.
+ *   causal   0 = full attention, nonzero = key j visible to query i iff j <= i.
+ *   scale    score multiplier, finite and > 0.
+ *   stream   cudaStream_t as void*.
+ *
+ * Returns FA2_OK once the kernel is enqueued; FA2_ERR_INVALID_ARG or
+ * FA2_ERR_UNSUPPORTED before touching the GPU when an argument is rejected;
+ * FA2_ERR_CUDA if building the TMA descriptors or the launch fails.
+ * Kernel-side wait time-outs are reported later by fa2_get_device_error().
+ */
+fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o,
+                   float *lse, int B, int H, int Lq, int Lk, int D,
+                   int causal, float scale, void *stream);
+
+/*
+ * fa2_fwd_from_host -- the same pass starting from, and ending in, HOST
+ * memory: enqueues on `stream` the host->device copies of q, k, v into the
+ * caller's device staging buffers, the kernel, and the device->host copies of
+ * O and LSE back into the caller's host buffers.  Host buffers should be
+ * pinned (page-locked) for the copies to be asynchronous.  The caller must
+ * synchronise `stream` before reading o_host / lse_host.
+ *
+ *   q_host .. lse_host   host pointers (same layouts as fa2_fwd).
+ *   q_dev  .. lse_dev    caller-owned device buffers of the same sizes.
+ *
+ * Errors: as fa2_fwd; FA2_ERR_CUDA if a copy cannot be enqueued.
+ */
+fa2_status fa2_fwd_from_host(const void *q_host, const void *k_host,
+                             const void *v_host, void *o_host, float *lse_host,
+                             void *q_dev, void *k_dev, void *v_dev, void *o_dev,
+                             float *lse_dev, int B, int H, int Lq, int Lk,
+                             int D, int causal, float scale, void *stream);
+
+/*
+ * fa2_get_device_error -- synchronises `stream`, then reads and clears the
+ * library's device-side error word on the current device.  Every inter-warp
+ * wait inside the kernels is bounded (about one second); a wait that runs out
+ * records a code here, the kernel winds down without hanging the GPU, and
+ * its outputs are undefined.
+ *
+ *   detail   optional (may be NULL): receives the raw code (0 = none).
+ *
+ * Returns FA2_OK, FA2_ERR_TIMEOUT, or FA2_ERR_CUDA if the synchronisation or
+ * the read fails.
+ */
+fa2_status fa2_get_device_error(void *stream, int *detail);
+
+/* Static human-readable name of a status code (never NULL). */
+const char *fa2_status_string(fa2_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int fa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_GB300_H */

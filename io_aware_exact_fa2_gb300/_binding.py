@@ -1,0 +1,122 @@
+"""ctypes binding to libfa2_gb300.so (declared in include/fa2.h).
+
+Argument marshalling only: shape/dtype checks, raw pointers, the current CUDA
+stream.  Every step of the forward pass runs in the library's kernels; there
+is no fallback.  Importing this module raises ImportError if the library has
+not been built (``python -m io_aware_exact_fa2_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+STATUS = {0: "FA2_OK", 1: "FA2_ERR_INVALID_ARG", 2: "FA2_ERR_UNSUPPORTED",
+          3: "FA2_ERR_CUDA", 4: "FA2_ERR_TIMEOUT"}
+
+
+class Fa2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where} failed: {STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"CUDA library {LIB_PATH} is missing: build it with "
+            "`python -m io_aware_exact_fa2_gb300.build` (there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa2_fwd.restype = i
+    lib.fa2_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.fa2_fwd_from_host.restype = i
+    lib.fa2_fwd_from_host.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp]
+    lib.fa2_get_device_error.restype = i
+    lib.fa2_get_device_error.argtypes = [vp, ctypes.POINTER(i)]
+    lib.fa2_status_string.restype = ctypes.c_char_p
+    lib.fa2_status_string.argtypes = [i]
+    lib.fa2_version.restype = i
+    lib.fa2_version.argtypes = []
+    return lib
+
+
+_lib = load_library()
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_shapes(q, k, v, o, lse):
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D (B, H, L, D)")
+    B, H, Lq, D = q.shape
+    if tuple(k.shape[:2]) != (B, H) or k.shape[3] != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if tuple(o.shape) != (B, H, Lq, D) or tuple(lse.shape) != (B, H, Lq):
+        raise ValueError("o must be (B, H, Lq, D) and lse (B, H, Lq)")
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("o", o, torch.bfloat16), ("lse", lse, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    return B, H, Lq, k.shape[2], D
+
+
+def fa2_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:
+    """Forward pass on CUDA tensors: writes o (bf16) and lse (fp32, natural log)."""
+    B, H, Lq, Lk, D = _check_shapes(q, k, v, o, lse)
+    for t in (q, k, v, o, lse):
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+    if scale is None:
+        scale = D ** -0.5
+    st = _lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      B, H, Lq, Lk, D, int(bool(causal)), float(scale), _stream_handle(stream, q.device))
+    if st != 0:
+        raise Fa2Error(st, "fa2_fwd")
+
+
+def fa2_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,
+                      causal: bool, scale: float | None = None, stream=None) -> None:
+    """Host buffers in, host buffers out (copies and kernel enqueued on `stream`).
+
+    The caller synchronises the stream before reading o_host / lse_host.
+    """
+    B, H, Lq, Lk, D = _check_shapes(q_host, k_host, v_host, o_host, lse_host)
+    _check_shapes(q_dev, k_dev, v_dev, o_dev, lse_dev)
+    if scale is None:
+        scale = D ** -0.5
+    st = _lib.fa2_fwd_from_host(
+        q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(), lse_host.data_ptr(),
+        q_dev.data_ptr(), k_dev.data_ptr(), v_dev.data_ptr(), o_dev.data_ptr(), lse_dev.data_ptr(),
+        B, H, Lq, Lk, D, int(bool(causal)), float(scale), _stream_handle(stream, q_dev.device))
+    if st != 0:
+        raise Fa2Error(st, "fa2_fwd_from_host")
+
+
+def fa2_get_device_error(stream=None) -> tuple[int, int]:
+    """Synchronise, then read and clear the kernels' error word: (status, raw code)."""
+    import torch
+    detail = ctypes.c_int(0)
+    st = _lib.fa2_get_device_error(_stream_handle(stream, torch.cuda.current_device()), ctypes.byref(detail))
+    return st, detail.value
+
+
+def fa2_status_string(status: int) -> str:
+    return _lib.fa2_status_string(int(status)).decode()
+
+
+def fa2_version() -> int:
+    return _lib.fa2_version()

@@ -1,0 +1,109 @@
+"""Build the CUDA library in-tree: io_aware_exact_fa2_gb300/libfa2_gb300.so.
+
+nvcc compiles each translation unit in csrc/ for sm_103a (in parallel), then
+links a shared library with the CUDA runtime linked statically and only the
+``fa2_*`` C symbols exported (a linker version script), so the library never
+interposes on, or binds to, another copy of the CUDA runtime in the process.
+
+    python -m io_aware_exact_fa2_gb300.build [--force] [--verbose]
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+LIB_NAME = "libfa2_gb300.so"
+LIB_PATH = os.path.join(PKG, LIB_NAME)
+SOURCES = ["fa2_api.cu", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu", "fa2_fwd_d256.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
+              "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xptxas", "-v",
+              "-I" + INCLUDE, "-I" + CSRC]
+
+
+def nvcc() -> str:
+    path = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(path):
+        raise RuntimeError("nvcc not found; the CUDA toolkit is required to build the library")
+    return path
+
+
+def source_digest() -> str:
+    """Hash of every kernel/host source and the public header (for staleness checks)."""
+    h = hashlib.sha256()
+    files = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    with open(os.path.join(INCLUDE, "fa2.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _stamp_path() -> str:
+    return os.path.join(BUILD, "digest.txt")
+
+
+def is_fresh() -> bool:
+    if not os.path.exists(LIB_PATH) or not os.path.exists(_stamp_path()):
+        return False
+    with open(_stamp_path()) as fh:
+        return fh.read().strip() == source_digest()
+
+
+def _compile(src: str, verbose: bool) -> str:
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    log = os.path.join(BUILD, os.path.splitext(src)[0] + ".ptxas.txt")
+    with open(log, "w") as fh:
+        fh.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+    if verbose:
+        sys.stdout.write(r.stderr)
+    return obj
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link the library unless it is already up to date. Returns its path."""
+    if not force and is_fresh():
+        return LIB_PATH
+    os.makedirs(BUILD, exist_ok=True)
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
+    vscript = os.path.join(BUILD, "exports.map")
+    with open(vscript, "w") as fh:
+        fh.write("{\n  global: fa2_*;\n  local: *;\n};\n")
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
+           "-Xlinker", f"--version-script={vscript}", "-Xlinker", "-Bsymbolic"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB_PATH)
+    with open(_stamp_path(), "w") as fh:
+        fh.write(source_digest())
+    return LIB_PATH
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--force", action="store_true")
+    ap.add_argument("--verbose", action="store_true")
+    args = ap.parse_args()
+    print(build(force=args.force, verbose=args.verbose))
+
+
+if __name__ == "__main__":
+    main()

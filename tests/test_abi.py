@@ -1,0 +1,121 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports exactly the
+entry points include/fa2.h declares, and rejects bad arguments on the host
+before any CUDA call.  (Compute calls are covered by the -m gpu tests.)"""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+from io_aware_exact_fa2_gb300 import build as fa2_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa2.h")
+
+OK, INVALID, UNSUPPORTED, CUDA_ERR, TIMEOUT = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = fa2_build.build()
+    from io_aware_exact_fa2_gb300 import _binding
+    assert _binding.library_path() == path
+    return _binding._lib
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa2_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert header_functions() == ["fa2_fwd", "fa2_fwd_from_host", "fa2_get_device_error",
+                                  "fa2_status_string", "fa2_version"]
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+@pytest.mark.skipif(shutil.which("nm") is None, reason="binutils nm not available")
+def test_library_exports_nothing_else(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa2_build.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = sorted({line.split()[-1] for line in out.splitlines()
+                       if line.split() and line.split()[-2] in ("T", "W", "D", "B")})
+    assert exported == header_functions()
+
+
+def test_status_strings_and_version(lib):
+    names = {OK: b"FA2_OK", INVALID: b"FA2_ERR_INVALID_ARG", UNSUPPORTED: b"FA2_ERR_UNSUPPORTED",
+             CUDA_ERR: b"FA2_ERR_CUDA", TIMEOUT: b"FA2_ERR_TIMEOUT"}
+    for code, name in names.items():
+        assert lib.fa2_status_string(code) == name
+    assert lib.fa2_status_string(99) == b"FA2_ERR_UNKNOWN"
+    assert lib.fa2_version() == 100
+
+
+# fake, never-dereferenced, 16-byte-aligned addresses: every case below must be
+# rejected by host-side validation before the library makes any CUDA call
+P = 0x10000
+
+
+def call(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, Lq=8, Lk=8, D=64, causal=0, scale=0.125):
+    return lib.fa2_fwd(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(v=0), INVALID),
+    (dict(o=0), INVALID), (dict(lse=0), INVALID),
+    (dict(q=P + 8), INVALID), (dict(k=P + 2), INVALID), (dict(v=P + 4), INVALID),
+    (dict(o=P + 1), INVALID), (dict(lse=P + 2), INVALID),
+    (dict(B=0), INVALID), (dict(H=-1), INVALID), (dict(Lq=-1), INVALID),
+    (dict(Lk=0), INVALID), (dict(D=0), INVALID),
+    (dict(B=65536, H=65536), INVALID),
+    (dict(scale=0.0), INVALID), (dict(scale=-0.5), INVALID),
+    (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(D=32), UNSUPPORTED), (dict(D=96), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
+    (dict(Lq=0), OK),
+])
+def test_host_validation(lib, kw, expect):
+    assert call(lib, **kw) == expect
+
+
+def test_from_host_validation(lib):
+    args = [P] * 10
+    f = lib.fa2_fwd_from_host
+    bad = list(args)
+    bad[0] = 0  # q_host
+    assert f(*bad, 1, 1, 8, 8, 64, 0, 0.125, None) == INVALID
+    bad = list(args)
+    bad[6] = P + 8  # k_dev misaligned
+    assert f(*bad, 1, 1, 8, 8, 64, 0, 0.125, None) == INVALID
+    assert f(*args, 1, 1, 8, 8, 80, 0, 0.125, None) == UNSUPPORTED
+    assert f(*args, 1, 1, 0, 8, 64, 0, 0.125, None) == OK
+
+
+def test_no_gpu_reports_cuda_error_instead_of_crashing(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible; this checks the no-device path")
+    assert call(lib) == CUDA_ERR
+
+
+def test_binding_shape_checks():
+    import torch
+    from io_aware_exact_fa2_gb300 import _binding
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 9, 64, dtype=torch.bfloat16)
+    o = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 8, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        _binding._check_shapes(q, k, k[:, :, :8], o, lse)
+    with pytest.raises(TypeError):
+        _binding._check_shapes(q.float(), k, k, o, lse)
+    with pytest.raises(ValueError):
+        _binding._check_shapes(q, k, k, o, lse[:, :, :7])
+    assert _binding._check_shapes(q, k, k, o, lse) == (1, 2, 8, 9, 64)
