@@ -61,11 +61,11 @@ def is_fresh() -> bool:
         return fh.read().strip() == source_digest()
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose: bool, build_dir: str, extra_flags) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
-    log = os.path.join(BUILD, os.path.splitext(src)[0] + ".ptxas.txt")
+    log = os.path.join(build_dir, os.path.splitext(src)[0] + ".ptxas.txt")
     with open(log, "w") as fh:
         fh.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
     if r.returncode != 0:
@@ -75,26 +75,35 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library unless it is already up to date. Returns its path."""
-    if not force and is_fresh():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), lib_path: str | None = None,
+          build_dir: str | None = None) -> str:
+    """Compile and link the library unless it is already up to date. Returns its path.
+
+    extra_flags / lib_path / build_dir build a separate copy (e.g. with -D tile
+    overrides for tuning) without touching the in-tree library.
+    """
+    default = lib_path is None and not extra_flags
+    if default and not force and is_fresh():
         return LIB_PATH
-    os.makedirs(BUILD, exist_ok=True)
+    out = LIB_PATH if lib_path is None else lib_path
+    bdir = BUILD if build_dir is None else build_dir
+    os.makedirs(bdir, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    vscript = os.path.join(BUILD, "exports.map")
+        objs = list(ex.map(lambda s: _compile(s, verbose, bdir, tuple(extra_flags)), SOURCES))
+    vscript = os.path.join(bdir, "exports.map")
     with open(vscript, "w") as fh:
         fh.write("{\n  global: fa2_*;\n  local: *;\n};\n")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
            "-Xlinker", f"--version-script={vscript}", "-Xlinker", "-Bsymbolic"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    with open(_stamp_path(), "w") as fh:
-        fh.write(source_digest())
-    return LIB_PATH
+    os.replace(tmp, out)
+    if default:
+        with open(_stamp_path(), "w") as fh:
+            fh.write(source_digest())
+    return out
 
 
 def main() -> None:

@@ -1,10 +1,31 @@
-// Forward kernel instantiation for head dimension 256: 1 Q tile(s) of 128 rows
-// per CTA, K/V tiles of 64 rows, a 2-stage K/V ring (sized so Q tiles + ring
-// fit the 227 KB shared-memory budget and S/P + O fit the 512 TMEM columns).
+// Forward kernel instantiation for head dimension 256: one 128-row Q tile per
+// CTA with two S buffers, K/V tiles of 64 rows, a 2-stage ring, one softmax
+// warp per row.
+// Q tiles + ring fit the 227 KB shared-memory budget and the O accumulators +
+// S buffers fit the 512 TMEM columns.  Defaults picked by measured c2/c3/c5
+// throughput on GB300.
 #include "fa2_launch.cuh"
 
 namespace fa2 {
 
-fa2_status launch_fwd_d256(const LaunchArgs &a) { return launch_fwd<FwdCfg<256, 64, 1, 2>>(a); }
+// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row);
+// overridable at compile time for tuning sweeps.
+#ifndef FA2_D256_BN
+#define FA2_D256_BN 64
+#endif
+#ifndef FA2_D256_NQ
+#define FA2_D256_NQ 1
+#endif
+#ifndef FA2_D256_KS
+#define FA2_D256_KS 2
+#endif
+#ifndef FA2_D256_CS
+#define FA2_D256_CS 1
+#endif
+
+fa2_status launch_fwd_d256(const LaunchArgs &a)
+{
+    return launch_fwd<FwdCfg<256, FA2_D256_BN, FA2_D256_NQ, FA2_D256_KS, FA2_D256_CS>>(a);
+}
 
 }  // namespace fa2

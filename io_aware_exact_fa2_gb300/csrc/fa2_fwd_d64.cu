@@ -1,10 +1,31 @@
-// Forward kernel instantiation for head dimension 64: 2 Q tile(s) of 128 rows
-// per CTA, K/V tiles of 128 rows, a 3-stage K/V ring (sized so Q tiles + ring
-// fit the 227 KB shared-memory budget and S/P + O fit the 512 TMEM columns).
+// Forward kernel instantiation for head dimension 64: two 128-row Q tiles per
+// CTA (one S buffer each), K/V tiles of 128 rows, a 3-stage ring, one softmax
+// warp per row.
+// Q tiles + ring fit the 227 KB shared-memory budget and the O accumulators +
+// S buffers fit the 512 TMEM columns.  Defaults picked by measured c2/c3/c5
+// throughput on GB300.
 #include "fa2_launch.cuh"
 
 namespace fa2 {
 
-fa2_status launch_fwd_d64(const LaunchArgs &a) { return launch_fwd<FwdCfg<64, 128, 2, 3>>(a); }
+// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row);
+// overridable at compile time for tuning sweeps.
+#ifndef FA2_D64_BN
+#define FA2_D64_BN 128
+#endif
+#ifndef FA2_D64_NQ
+#define FA2_D64_NQ 2
+#endif
+#ifndef FA2_D64_KS
+#define FA2_D64_KS 3
+#endif
+#ifndef FA2_D64_CS
+#define FA2_D64_CS 1
+#endif
+
+fa2_status launch_fwd_d64(const LaunchArgs &a)
+{
+    return launch_fwd<FwdCfg<64, FA2_D64_BN, FA2_D64_NQ, FA2_D64_KS, FA2_D64_CS>>(a);
+}
 
 }  // namespace fa2

@@ -3,7 +3,7 @@
 // The method (Olowookere, "FlashAttention-2 from scratch with a custom Triton
 // kernel", sections "The core idea: making attention IO-aware" and "Running
 // max m_i and running normaliser"; "Chapter 08: Flash Attention -- blocked
-// attention", sections 1-5): one CTA owns NQ query tiles of 128 rows of one
+// attention", sections 1-5): a CTA owns NQ query tiles of 128 rows of one
 // (batch, head); the tiles stay on chip while K/V tiles of BN rows stream
 // through shared memory; per row the kernel keeps a running max m, a running
 // normaliser l and an unnormalised accumulator O, rescales O and l when m
@@ -13,23 +13,28 @@
 // never visited and only tiles that straddle the diagonal (or the key tail)
 // pay for element masking.
 //
-// GB300 mapping (prior art on the pages is Triton on A100/Ada; this is not a
-// translation of it):
+// GB300 mapping (the pages' kernels are Triton for A100/Ada; this is not a
+// translation of them):
 //   * TMA (cp.async.bulk.tensor, 128B swizzle) moves Q once and K/V per tile
 //     into a KS-stage shared-memory ring guarded by mbarriers.
-//   * One thread issues tcgen05.mma: S = Q K^T into TMEM (fp32), then
+//   * One warp issues tcgen05.mma (a single elected lane, warp-uniform control
+//     flow, descriptors precomputed): S = Q K^T into TMEM (fp32), then
 //     O += P V with P read straight from TMEM (bf16, aliasing S) and V from
-//     shared memory (MN-major operand: no transpose pass).
-//   * One warpgroup per Q tile (thread <-> row, TMEM lane == row) runs the
-//     online softmax out of TMEM, writes P back to TMEM, and rescales O in
-//     TMEM only when a row's max grows by more than 2^8 (the stale max is
-//     kept otherwise, which is exact because l and LSE use the same max).
+//     shared memory as an MN-major operand (no transpose pass).  With one Q
+//     tile per CTA each tile has two S buffers, so S(j+1) is computed while
+//     the softmax of tile j runs.
+//   * Softmax: CS warps share each row (TMEM lane == row; warp w may touch
+//     lanes 32*(w%4)..+31), each owning BN/CS columns of S and D/CS columns
+//     of O.  The row max is exchanged through shared memory every tile; the
+//     warps write P back to TMEM and rescale O in TMEM only when a row's max
+//     grows by more than 2^8 (the stale max is kept otherwise, which is exact
+//     because l and LSE use the same max).
 //   * The epilogue multiplies by 1/l, packs bf16 into the (now free) Q tile
-//     in the swizzled layout and stores it with TMA (one 32-row box per warp;
-//     rows >= Lq are clipped by the tensor bounds); LSE goes out as
-//     coalesced fp32 stores.
-//   * Every inter-warp wait is bounded in time; a wait that runs out records
-//     a code in a device error word and the CTA winds down.
+//     in the swizzled layout and stores it with TMA (rows >= Lq are clipped
+//     by the tensor bounds); LSE goes out as coalesced fp32 stores.
+//   * Every wait between warps is on an mbarrier with a time bound; a wait
+//     that runs out records a code in a device error word and the CTA winds
+//     down, so no input can hang the GPU.
 #pragma once
 
 #include <cstdint>
@@ -62,14 +67,17 @@ enum : int {
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.69314718055994530942f;
 
-template <int D_, int BN_, int NQ_, int KS_>
+template <int D_, int BN_, int NQ_, int KS_, int CS_>
 struct FwdCfg {
     static constexpr int D = D_;     // head dimension
     static constexpr int BN = BN_;   // K/V rows per tile
-    static constexpr int NQ = NQ_;   // 128-row Q tiles per CTA (one softmax warpgroup each)
+    static constexpr int NQ = NQ_;   // 128-row Q tiles per CTA
     static constexpr int KS = KS_;   // K/V ring stages
+    static constexpr int CS = CS_;   // softmax warps sharing one row (column split)
     static constexpr int BM = 128;   // Q rows per tile = TMEM lanes = MMA M
     static constexpr int NS = (NQ == 1) ? 2 : 1;  // S/P TMEM buffers per Q tile
+    static constexpr int NCOL = BN / CS;          // S columns per softmax thread
+    static constexpr int OCOL = D / CS;           // O columns per softmax thread
     static constexpr int DB = D / 64;             // 64-column (128-byte) swizzle blocks
     static constexpr int Q_BLOCK = BM * 128;
     static constexpr int KV_BLOCK = BN * 128;
@@ -80,16 +88,20 @@ struct FwdCfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
-    static constexpr int OFF_BAR = OFF_V + KS * KV_TILE;
+    static constexpr int OFF_XMAX = OFF_V + KS * KV_TILE;           // f32 [NQ][2][CS][128]
+    static constexpr int OFF_XL = OFF_XMAX + NQ * 2 * CS * 128 * 4;  // f32x2 [NQ][CS][128]
+    static constexpr int OFF_BAR = OFF_XL + NQ * CS * 128 * 8;
     static constexpr int BAR_Q = 0;
     static constexpr int BAR_K_FULL = 1;
     static constexpr int BAR_K_EMPTY = BAR_K_FULL + KS;
     static constexpr int BAR_V_FULL = BAR_K_EMPTY + KS;
     static constexpr int BAR_V_EMPTY = BAR_V_FULL + KS;
-    static constexpr int BAR_S_FULL = BAR_V_EMPTY + KS;   // [NQ][NS]
+    static constexpr int BAR_S_FULL = BAR_V_EMPTY + KS;      // [NQ][NS]
     static constexpr int BAR_O_DONE = BAR_S_FULL + NQ * NS;  // [NQ]
-    static constexpr int BAR_P_READY = BAR_O_DONE + NQ;      // [NQ]
-    static constexpr int BAR_DRAIN = BAR_P_READY + NQ;
+    static constexpr int BAR_P_READY = BAR_O_DONE + NQ;      // [NQ][NS]
+    static constexpr int BAR_XMAX = BAR_P_READY + NQ * NS;   // [NQ][2]
+    static constexpr int BAR_GROUP = BAR_XMAX + 2 * NQ;      // [NQ]
+    static constexpr int BAR_DRAIN = BAR_GROUP + NQ;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;  // + slack for base alignment
@@ -101,17 +113,29 @@ struct FwdCfg {
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
                                    : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
 
-    // warp roles
-    static constexpr int NUM_SOFTMAX_WARPS = 4 * NQ;
+    // warp roles: softmax warpgroups first, then a control warpgroup (TMA
+    // producer warp, MMA warp and, when registers are re-split, two idle warps)
+    static constexpr int GROUP_THREADS = 128 * CS;             // softmax threads per Q tile
+    static constexpr int NUM_SOFTMAX_WARPS = 4 * CS * NQ;
     static constexpr int WARP_PRODUCER = NUM_SOFTMAX_WARPS;
     static constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;
-    static constexpr int NUM_THREADS = 32 * (NUM_SOFTMAX_WARPS + 2);
+    // With two softmax warpgroups the launch leaves 168 registers per thread; the
+    // control warpgroup drops to REG_CTRL and the softmax warpgroups rise to
+    // REG_SOFTMAX.  Budget: 2*128*208 + 128*88 = 64512 = 384 threads * 168.
+    static constexpr bool REG_SPLIT = (NUM_SOFTMAX_WARPS == 8);
+    static constexpr int REG_SOFTMAX = 208;
+    static constexpr int REG_CTRL = 88;
+    static constexpr int NUM_THREADS = 32 * (NUM_SOFTMAX_WARPS + (REG_SPLIT ? 4 : 2));
+    static_assert(!REG_SPLIT || 2 * 128 * REG_SOFTMAX + 128 * REG_CTRL <= NUM_THREADS * 168,
+                  "register split exceeds the launch allocation");
 
     static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false, false);
     static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, false, true);
 
     static_assert(D % 64 == 0 && D >= 64 && D <= 256, "D must be 64, 128 or 256");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64, 256]");
+    static_assert(CS == 1 || CS == 2, "one or two warps per row");
+    static_assert(NCOL % 32 == 0 && OCOL % 32 == 0, "per-thread column slices are whole 32-column loads");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
@@ -187,11 +211,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_init(bar(C::BAR_V_FULL + s), 1);
             mbar_init(bar(C::BAR_V_EMPTY + s), 1);
         }
-        for (int i = 0; i < C::NQ * C::NS; ++i)
+        for (int i = 0; i < C::NQ * C::NS; ++i) {
             mbar_init(bar(C::BAR_S_FULL + i), 1);
+            mbar_init(bar(C::BAR_P_READY + i), C::GROUP_THREADS);
+        }
         for (int t = 0; t < C::NQ; ++t) {
             mbar_init(bar(C::BAR_O_DONE + t), 1);
-            mbar_init(bar(C::BAR_P_READY + t), 128);
+            mbar_init(bar(C::BAR_XMAX + 2 * t), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_XMAX + 2 * t + 1), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_GROUP + t), C::GROUP_THREADS);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
         fence_mbar_init();
@@ -206,8 +234,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const uint32_t tmem =
         *reinterpret_cast<volatile uint32_t *>(smem_raw + (sbase - raw) + C::OFF_TMEM_SLOT);
 
-    if (warp == C::WARP_PRODUCER) {
-        // ================================================== TMA producer
+    if (warp >= C::NUM_SOFTMAX_WARPS) {
+      // control warpgroup: every warp of it gives up registers at the same point
+      if constexpr (C::REG_SPLIT)
+          setmaxnreg_dec<C::REG_CTRL>();
+      if (warp == C::WARP_PRODUCER) {
+        // ================================================== TMA producer (one lane)
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -261,82 +293,104 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == C::WARP_MMA) {
-        // ================================================== MMA issuer (one thread)
-        if (lane == 0) {
-            bool ok = mbar_wait(bar(C::BAR_Q), 0, p.err, ERR_MMA | 1, p.wait_limit_ns);
-            tc_fence_after();
+        // ================================================== MMA issuer
+        // The whole warp runs the (uniform) control flow and the waits; one
+        // elected lane issues the MMAs and commits.
+        const bool leader = elect_one();
+        bool ok = warp_wait(bar(C::BAR_Q), 0, p.err, ERR_MMA | 1, p.wait_limit_ns);
+        tc_fence_after();
+        // Descriptor bases; a K step moves the start address, which is the low
+        // field of the descriptor in 16-byte units, so it is a plain add.
+        const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+        const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+        const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_V, C::KV_BLOCK, 1024);
 
-            // S(t, j) = Q_t K_j^T  into S/P buffer (t, j % NS)
-            auto issue_s = [&](int t, int j) -> bool {
-                const int s = j % C::KS;
-                if (!mbar_wait(bar(C::BAR_K_FULL + s), (j / C::KS) & 1, p.err, ERR_MMA | 2, p.wait_limit_ns))
-                    return false;
-                tc_fence_after();
+        // S(t, j) = Q_t K_j^T  into S/P buffer (t, j % NS)
+        auto issue_s = [&](int t, int j) -> bool {
+            const int s = j % C::KS;
+            if (!warp_wait(bar(C::BAR_K_FULL + s), (j / C::KS) & 1, p.err, ERR_MMA | 2, p.wait_limit_ns))
+                return false;
+            tc_fence_after();
+            if (leader) {
                 const uint32_t d = tmem + C::TM_S + (t * C::NS + j % C::NS) * C::BN;
-                const uint32_t qa = sbase + C::OFF_Q + t * C::Q_TILE;
-                const uint32_t kb = sbase + C::OFF_K + s * C::KV_TILE;
+                const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
+                const uint64_t dk = desc_k + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < C::D / 16; ++kk) {
-                    const uint32_t oq = (kk >> 2) * C::Q_BLOCK + (kk & 3) * 32;
-                    const uint32_t ok_ = (kk >> 2) * C::KV_BLOCK + (kk & 3) * 32;
-                    mma_ss(d, sdesc_sw128(qa + oq, 16, 1024), sdesc_sw128(kb + ok_, 16, 1024), C::IDESC_S,
-                           kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < C::D / 16; ++kk)
+                    mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
+                           dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
+                           C::IDESC_S, kk > 0 ? 1u : 0u);
                 mma_commit(bar(C::BAR_S_FULL + t * C::NS + j % C::NS));
                 if (last_user(j) == t)
                     mma_commit(bar(C::BAR_K_EMPTY + s));
-                return true;
-            };
-            // O_t (+)= P(t, j) V_j, P read from TMEM
-            auto issue_pv = [&](int t, int j) -> bool {
-                const int s = j % C::KS;
-                if (!mbar_wait(bar(C::BAR_P_READY + t), j & 1, p.err, ERR_MMA | 3, p.wait_limit_ns))
-                    return false;
-                if (!mbar_wait(bar(C::BAR_V_FULL + s), (j / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
-                    return false;
-                tc_fence_after();
+            }
+            __syncwarp();
+            return true;
+        };
+        // O_t (+)= P(t, j) V_j, P read from TMEM
+        auto issue_pv = [&](int t, int j) -> bool {
+            const int s = j % C::KS;
+            if (!warp_wait(bar(C::BAR_P_READY + t * C::NS + j % C::NS), (j / C::NS) & 1, p.err, ERR_MMA | 3,
+                           p.wait_limit_ns))
+                return false;
+            if (!warp_wait(bar(C::BAR_V_FULL + s), (j / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
+                return false;
+            tc_fence_after();
+            if (leader) {
                 const uint32_t d = tmem + C::TM_O + t * C::D;
                 const uint32_t a = tmem + C::TM_S + (t * C::NS + j % C::NS) * C::BN;
-                const uint32_t vb = sbase + C::OFF_V + s * C::KV_TILE;
+                const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
-                    mma_ts(d, a + kk * 8, sdesc_sw128(vb + kk * 2048, C::KV_BLOCK, 1024), C::IDESC_PV,
+                    mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
                            (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(C::BAR_O_DONE + t));
                 if (last_user(j) == t)
                     mma_commit(bar(C::BAR_V_EMPTY + s));
-                return true;
-            };
+            }
+            __syncwarp();
+            return true;
+        };
 
-            // Issue order: S for the first NS tiles of every Q tile, then per K/V
-            // tile j and Q tile t: PV(t, j) followed by S(t, j + NS), which reuses
-            // the TMEM buffer PV(t, j) just read (tcgen05 ops execute in order).
-            for (int b = 0; b < C::NS && ok; ++b)
-                for (int t = 0; t < C::NQ && ok; ++t)
-                    if (b < n_of(t))
-                        ok = issue_s(t, b);
-            for (int j = 0; j < n_max && ok; ++j)
-                for (int t = 0; t < C::NQ && ok; ++t)
-                    if (j < n_of(t)) {
-                        ok = issue_pv(t, j);
-                        if (ok && j + C::NS < n_of(t))
-                            ok = issue_s(t, j + C::NS);
-                    }
-            // drain: every MMA issued above has completed before TMEM can be released
-            mma_commit(bar(C::BAR_DRAIN));
-            mbar_wait(bar(C::BAR_DRAIN), 0, p.err, ERR_DRAIN | 4, p.wait_limit_ns);
+        // Issue order: S for the first NS tiles of every Q tile, then per K/V
+        // tile j and Q tile t: PV(t, j) followed by S(t, j + NS), which reuses
+        // the TMEM buffer PV(t, j) just read (tcgen05 ops execute in order).
+#pragma unroll
+        for (int b = 0; b < C::NS; ++b)
+#pragma unroll
+            for (int t = 0; t < C::NQ; ++t)
+                if (ok && b < n_of(t))
+                    ok = issue_s(t, b);
+        for (int j = 0; j < n_max && ok; ++j) {
+#pragma unroll
+            for (int t = 0; t < C::NQ; ++t) {
+                if (ok && j < n_of(t)) {
+                    ok = issue_pv(t, j);
+                    if (ok && j + C::NS < n_of(t))
+                        ok = issue_s(t, j + C::NS);
+                }
+            }
         }
+        // drain: every MMA issued above has completed before TMEM can be released
+        if (leader)
+            mma_commit(bar(C::BAR_DRAIN));
         __syncwarp();
+        warp_wait(bar(C::BAR_DRAIN), 0, p.err, ERR_DRAIN | 4, p.wait_limit_ns);
+      }
     } else {
-        // ================================================== softmax warpgroups
-        const int t = warp >> 2;        // Q tile
-        const int quarter = warp & 3;   // TMEM lane quarter this warp may access
+        // ================================================== softmax warps
+        if constexpr (C::REG_SPLIT)
+            setmaxnreg_inc<C::REG_SOFTMAX>();
+        const int t = warp / (4 * C::CS);        // Q tile
+        const int h = (warp >> 2) % C::CS;       // column slice
+        const int quarter = warp & 3;            // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
         const int q0_t = q0 + t * C::BM;
-        const int grow = q0_t + row;    // query index
+        const int grow = q0_t + row;             // query index
         const int n = n_of(t);
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t o_addr = tmem + lane_base + C::TM_O + t * C::D;
+        const uint32_t o_addr = tmem + lane_base + C::TM_O + t * C::D + h * C::OCOL;
+        const uint32_t xmax = sbase + C::OFF_XMAX + t * (2 * C::CS * 128 * 4);
         const float c2 = p.scale_log2;
         float m_use = -INFINITY;   // running max (log2 domain, possibly stale by < 2^THRESHOLD)
         float l = 0.f;             // running normaliser of the fp32 weights (for LSE)
@@ -352,45 +406,63 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t s_addr = tmem + lane_base + C::TM_S + (t * C::NS + b) * C::BN;
 
-            float s[C::BN];
+            float s[C::NCOL];
             {
-                uint32_t r[C::BN / 32][32];
+                uint32_t r[C::NCOL / 32][32];
 #pragma unroll
-                for (int q = 0; q < C::BN / 32; ++q)
-                    tmem_ld32(s_addr + 32 * q, r[q]);
+                for (int q = 0; q < C::NCOL / 32; ++q)
+                    tmem_ld32(s_addr + h * C::NCOL + 32 * q, r[q]);
 #pragma unroll
-                for (int q = 0; q < C::BN / 32; ++q)
+                for (int q = 0; q < C::NCOL / 32; ++q)
                     tmem_ld_wait(r[q]);
 #pragma unroll
-                for (int q = 0; q < C::BN / 32; ++q)
+                for (int q = 0; q < C::NCOL / 32; ++q)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         s[32 * q + i] = __uint_as_float(r[q][i]);
             }
 
             // mask: key tail (j >= Lk) and, on tiles crossing the diagonal, causal j > i
-            const int k0 = j * C::BN;
-            if ((p.causal && k0 + C::BN - 1 > q0_t) || (k0 + C::BN > p.Lk)) {
+            const int k0 = j * C::BN + h * C::NCOL;
+            if ((p.causal && j * C::BN + C::BN - 1 > q0_t) || (j * C::BN + C::BN > p.Lk)) {
                 const int lim = p.causal ? min(grow + 1, p.Lk) : p.Lk;  // keys < lim are visible
 #pragma unroll
-                for (int c = 0; c < C::BN; ++c)
+                for (int c = 0; c < C::NCOL; ++c)
                     if (k0 + c >= lim)
                         s[c] = -INFINITY;
             }
 
-            // row max of this tile, in the scaled log2 domain
+            // row max of this tile (own slice, then the other slices through shared
+            // memory): four independent chains of 3-input maxima
             float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-            for (int c = 4; c < C::BN; c += 4) {
-                mx0 = fmaxf(mx0, s[c]);
-                mx1 = fmaxf(mx1, s[c + 1]);
-                mx2 = fmaxf(mx2, s[c + 2]);
-                mx3 = fmaxf(mx3, s[c + 3]);
+            for (int c = 4; c < C::NCOL; c += 8) {
+                mx0 = max3(mx0, s[c], s[c + 1]);
+                mx1 = max3(mx1, s[c + 2], s[c + 3]);
+                if (c + 4 < C::NCOL) {
+                    mx2 = max3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = max3(mx3, s[c + 6], s[c + 7]);
+                }
             }
-            const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+            float mx = fmaxf(max3(mx0, mx1, mx2), mx3);
+            if constexpr (C::CS > 1) {
+                const uint32_t xb = xmax + (j & 1) * (C::CS * 128 * 4);
+                st_shared_f32(xb + (h * 128 + row) * 4, mx);
+                mbar_arrive(bar(C::BAR_XMAX + 2 * t + (j & 1)));
+                ok = warp_wait(bar(C::BAR_XMAX + 2 * t + (j & 1)), (j >> 1) & 1, p.err, ERR_SOFTMAX | 4,
+                               p.wait_limit_ns);
+                if (!ok)
+                    break;
+#pragma unroll
+                for (int hh = 0; hh < C::CS; ++hh)
+                    if (hh != h)
+                        mx = fmaxf(mx, ld_shared_f32(xb + (hh * 128 + row) * 4));
+            }
+            const float m_tile = mx * c2;
 
             // The first tile always holds key 0, which every row may see, so m_tile is
-            // finite there; later tiles keep the stale max unless it grows a lot.
+            // finite there; later tiles keep the stale max unless it grows a lot.  All
+            // slices of a row see the same m_tile and so take the same decision.
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -403,41 +475,69 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
             // p = 2^(s * scale * log2e - m); masked entries give 2^-inf = 0.  P goes to
             // TMEM as bf16 (two per 32-bit column, over the first BN/2 columns of the S
-            // buffer).  Two normalisers are kept: l sums the fp32 p (LSE needs the exact
-            // sum) and l_o sums the bf16-rounded p that the PV MMA multiplies, so O's
-            // numerator and denominator use the same weights -- with one dominant key
-            // the rounding of its weight then cancels instead of showing up in O.
-            const float neg_m = -m_use;
-            float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+            // buffer; this slice's keys land in columns h*NCOL/2 ..).  Two normalisers
+            // are kept: l sums the fp32 p (LSE needs the exact sum) and l_o sums the
+            // bf16-rounded p that the PV MMA multiplies, so O's numerator and
+            // denominator use the same weights -- with one dominant key the rounding
+            // of its weight then cancels instead of showing up in O.
+            // (scale and subtract, and the exact sum, run as packed fp32 pairs)
+            const uint64_t c2x2 = f32x2(c2, c2);
+            const uint64_t negm2 = f32x2(-m_use, -m_use);
+            uint64_t ls01 = 0, ls23 = 0;   // packed (0.f, 0.f)
+            float lr0 = 0.f, lr1 = 0.f;
             {
-                uint32_t pk[C::BN / 64][32];
+                uint32_t pk[C::NCOL / 2];
 #pragma unroll
-                for (int c = 0; c < C::BN; c += 2) {
-                    const float p0 = ex2_approx(fmaf(s[c], c2, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[c + 1], c2, neg_m));
-                    const uint32_t w = pack_bf16x2(p0, p1);
-                    pk[(c / 2) / 32][(c / 2) % 32] = w;
-                    ls0 += p0;
-                    ls1 += p1;
-                    lr0 += __uint_as_float(w << 16);
-                    lr1 += __uint_as_float(w & 0xFFFF0000u);
+                for (int c = 0; c < C::NCOL; c += 4) {
+                    float x0, x1, x2, x3;
+                    unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), c2x2, negm2), x0, x1);
+                    unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), c2x2, negm2), x2, x3);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    const float p2 = ex2_approx(x2);
+                    const float p3 = ex2_approx(x3);
+                    const uint32_t w0 = pack_bf16x2(p0, p1);
+                    const uint32_t w1 = pack_bf16x2(p2, p3);
+                    pk[c / 2] = w0;
+                    pk[c / 2 + 1] = w1;
+                    ls01 = add_f32x2(ls01, f32x2(p0, p1));
+                    ls23 = add_f32x2(ls23, f32x2(p2, p3));
+                    lr0 = add_bf16x2_to_f32(lr0, w0);
+                    lr1 = add_bf16x2_to_f32(lr1, w1);
                 }
+                const uint32_t p_addr = s_addr + h * (C::NCOL / 2);
+                if constexpr (C::NCOL / 2 >= 32) {
 #pragma unroll
-                for (int q = 0; q < C::BN / 64; ++q)
-                    tmem_st32(s_addr + 32 * q, pk[q]);
+                    for (int q = 0; q < C::NCOL / 64; ++q)
+                        tmem_st32(p_addr + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * q));
+                } else {
+                    tmem_st16(p_addr, pk);
+                }
             }
-            l = l * alpha + (ls0 + ls1);
+            {
+                float a0, a1, a2, a3;
+                unpack_f32x2(ls01, a0, a1);
+                unpack_f32x2(ls23, a2, a3);
+                l = l * alpha + ((a0 + a1) + (a2 + a3));
+            }
             l_o = l_o * alpha + (lr0 + lr1);
 
-            // rescale O once the previous PV has landed (only warps with a grown max)
-            if (j > 0) {
+            // Rescale this slice of O (only warps in which some row's max grew) once
+            // the previous PV has landed.  Without a rescale there is nothing to wait
+            // for: the MMA warp orders PV(j) after PV(j-1) by itself.  A parity wait on
+            // O_DONE is only unambiguous while that barrier is at most one phase behind
+            // the awaited one: here S(j) completing implies PV(j - NS) completed, so
+            // waiting for PV(j-1) is safe; and the wait at the last tile (taken even
+            // without a rescale) keeps the epilogue's wait for PV(n-1) safe too.
+            const bool grow_any = __any_sync(0xffffffffu, rescale);
+            if (j > 0 && (grow_any || j == n - 1)) {
                 ok = warp_wait(bar(C::BAR_O_DONE + t), (j - 1) & 1, p.err, ERR_SOFTMAX | 2, p.wait_limit_ns);
                 if (!ok)
                     break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+                if (grow_any) {
 #pragma unroll 1
-                    for (int cc = 0; cc < C::D / 32; ++cc) {
+                    for (int cc = 0; cc < C::OCOL / 32; ++cc) {
                         uint32_t r[32];
                         tmem_ld32(o_addr + 32 * cc, r);
                         tmem_ld_wait(r);
@@ -450,19 +550,41 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(C::BAR_P_READY + t));
+            // P_READY is per S buffer: the softmax may finish tile j+1 before the MMA
+            // warp has seen tile j, but it can only reuse a buffer after the MMA warp
+            // issued the S that refills it, i.e. after it consumed that buffer's P.
+            mbar_arrive(bar(C::BAR_P_READY + t * C::NS + b));
         }
 
         // ---- epilogue: O / l -> bf16 -> swizzled smem (the Q tile) -> TMA store; LSE
         if (ok && n > 0) {
             ok = warp_wait(bar(C::BAR_O_DONE + t), (n - 1) & 1, p.err, ERR_SOFTMAX | 3, p.wait_limit_ns);
+            float l_tot = l, lo_tot = l_o;
+            const uint32_t xl = sbase + C::OFF_XL + t * (C::CS * 128 * 8);
+            if constexpr (C::CS > 1) {
+                if (ok) {
+                    st_shared_f32(xl + (h * 128 + row) * 8, l);
+                    st_shared_f32(xl + (h * 128 + row) * 8 + 4, l_o);
+                    mbar_arrive(bar(C::BAR_GROUP + t));
+                    ok = warp_wait(bar(C::BAR_GROUP + t), 0, p.err, ERR_SOFTMAX | 5, p.wait_limit_ns);
+                    if (ok) {
+                        l_tot = 0.f;
+                        lo_tot = 0.f;
+#pragma unroll
+                        for (int hh = 0; hh < C::CS; ++hh) {
+                            l_tot += ld_shared_f32(xl + (hh * 128 + row) * 8);
+                            lo_tot += ld_shared_f32(xl + (hh * 128 + row) * 8 + 4);
+                        }
+                    }
+                }
+            }
             if (ok) {
                 tc_fence_after();
-                const float inv_l = 1.f / l_o;
-                const float lse = (m_use + lg2_approx(l)) * LN2;
+                const float inv_l = 1.f / lo_tot;
+                const float lse = (m_use + lg2_approx(l_tot)) * LN2;
                 const uint32_t stage = sbase + C::OFF_Q + t * C::Q_TILE;
 #pragma unroll 1
-                for (int cc = 0; cc < C::D / 32; ++cc) {
+                for (int cc = 0; cc < C::OCOL / 32; ++cc) {
                     uint32_t r[32];
                     tmem_ld32(o_addr + 32 * cc, r);
                     tmem_ld_wait(r);
@@ -470,17 +592,25 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-                    const uint32_t row_addr = stage + (cc >> 1) * C::Q_BLOCK + row * 128;
-                    const int chunk0 = (cc & 1) * 4;
+                    const int col0 = h * C::OCOL + 32 * cc;  // first O column of this chunk
+                    const uint32_t row_addr = stage + (col0 >> 6) * C::Q_BLOCK + row * 128;
+                    const int chunk0 = (col0 & 63) >> 3;     // first 16-byte chunk within the 128-byte row
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         st_shared_v4(row_addr + (((chunk0 + q) ^ (row & 7)) << 4), w[4 * q], w[4 * q + 1],
                                      w[4 * q + 2], w[4 * q + 3]);
                 }
                 fence_proxy_async_smem();
-                __syncwarp();
+                if constexpr (C::CS > 1) {
+                    mbar_arrive(bar(C::BAR_GROUP + t));
+                    if (h == 0)
+                        ok = warp_wait(bar(C::BAR_GROUP + t), 1, p.err, ERR_SOFTMAX | 6, p.wait_limit_ns);
+                } else {
+                    __syncwarp();
+                }
+                // the slice-0 warp of each lane quarter stores the quarter's 32 rows
                 const int r0 = q0_t + quarter * 32;
-                if (lane == 0 && r0 < p.Lq) {
+                if (ok && h == 0 && lane == 0 && r0 < p.Lq) {
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
                         tma_store_3d(&tm_o, 64 * c, r0, bh, stage + c * C::Q_BLOCK + quarter * 32 * 128);
@@ -488,7 +618,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     tma_store_wait_read_all();
                 }
                 __syncwarp();
-                if (grow < p.Lq)
+                if (ok && h == 0 && grow < p.Lq)
                     p.lse[static_cast<size_t>(bh) * p.Lq + grow] = lse;
             }
         }
