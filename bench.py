@@ -100,8 +100,14 @@ class ClockSampler:
             self.proc.wait(timeout=2)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summarize(self.lines, t0, t1)
+
+    @staticmethod
+    def summarize(lines, t0: float, t1: float):
+        """Median SM clock, max clock, throttle reasons seen, from (time, csv line) samples
+        taken within [t0, t1] (all samples if none fall inside)."""
         rows = []
-        for ts, line in self.lines:
+        for ts, line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
