@@ -8,7 +8,8 @@
 
 namespace fa2 {
 
-// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row);
+// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row,
+// S buffers per Q tile);
 // overridable at compile time for tuning sweeps.
 #ifndef FA2_D128_BN
 #define FA2_D128_BN 128
@@ -19,13 +20,16 @@ namespace fa2 {
 #ifndef FA2_D128_KS
 #define FA2_D128_KS 2
 #endif
+#ifndef FA2_D128_NS
+#define FA2_D128_NS (FA2_D128_NQ == 1 ? 2 : 1)
+#endif
 #ifndef FA2_D128_CS
 #define FA2_D128_CS 1
 #endif
 
 fa2_status launch_fwd_d128(const LaunchArgs &a)
 {
-    return launch_fwd<FwdCfg<128, FA2_D128_BN, FA2_D128_NQ, FA2_D128_KS, FA2_D128_CS>>(a);
+    return launch_fwd<FwdCfg<128, FA2_D128_BN, FA2_D128_NQ, FA2_D128_KS, FA2_D128_CS, FA2_D128_NS>>(a);
 }
 
 }  // namespace fa2

@@ -8,7 +8,8 @@
 
 namespace fa2 {
 
-// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row);
+// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row,
+// S buffers per Q tile);
 // overridable at compile time for tuning sweeps.
 #ifndef FA2_D256_BN
 #define FA2_D256_BN 64
@@ -19,13 +20,16 @@ namespace fa2 {
 #ifndef FA2_D256_KS
 #define FA2_D256_KS 2
 #endif
+#ifndef FA2_D256_NS
+#define FA2_D256_NS (FA2_D256_NQ == 1 ? 2 : 1)
+#endif
 #ifndef FA2_D256_CS
 #define FA2_D256_CS 1
 #endif
 
 fa2_status launch_fwd_d256(const LaunchArgs &a)
 {
-    return launch_fwd<FwdCfg<256, FA2_D256_BN, FA2_D256_NQ, FA2_D256_KS, FA2_D256_CS>>(a);
+    return launch_fwd<FwdCfg<256, FA2_D256_BN, FA2_D256_NQ, FA2_D256_KS, FA2_D256_CS, FA2_D256_NS>>(a);
 }
 
 }  // namespace fa2

@@ -8,7 +8,8 @@
 
 namespace fa2 {
 
-// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row);
+// Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row,
+// S buffers per Q tile);
 // overridable at compile time for tuning sweeps.
 #ifndef FA2_D64_BN
 #define FA2_D64_BN 128
@@ -19,13 +20,16 @@ namespace fa2 {
 #ifndef FA2_D64_KS
 #define FA2_D64_KS 3
 #endif
+#ifndef FA2_D64_NS
+#define FA2_D64_NS (FA2_D64_NQ == 1 ? 2 : 1)
+#endif
 #ifndef FA2_D64_CS
 #define FA2_D64_CS 1
 #endif
 
 fa2_status launch_fwd_d64(const LaunchArgs &a)
 {
-    return launch_fwd<FwdCfg<64, FA2_D64_BN, FA2_D64_NQ, FA2_D64_KS, FA2_D64_CS>>(a);
+    return launch_fwd<FwdCfg<64, FA2_D64_BN, FA2_D64_NQ, FA2_D64_KS, FA2_D64_CS, FA2_D64_NS>>(a);
 }
 
 }  // namespace fa2

@@ -67,7 +67,7 @@ enum : int {
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.69314718055994530942f;
 
-template <int D_, int BN_, int NQ_, int KS_, int CS_>
+template <int D_, int BN_, int NQ_, int KS_, int CS_, int NS_ = (NQ_ == 1 ? 2 : 1)>
 struct FwdCfg {
     static constexpr int D = D_;     // head dimension
     static constexpr int BN = BN_;   // K/V rows per tile
@@ -75,7 +75,7 @@ struct FwdCfg {
     static constexpr int KS = KS_;   // K/V ring stages
     static constexpr int CS = CS_;   // softmax warps sharing one row (column split)
     static constexpr int BM = 128;   // Q rows per tile = TMEM lanes = MMA M
-    static constexpr int NS = (NQ == 1) ? 2 : 1;  // S/P TMEM buffers per Q tile
+    static constexpr int NS = NS_;                // S/P TMEM buffers per Q tile
     static constexpr int NCOL = BN / CS;          // S columns per softmax thread
     static constexpr int OCOL = D / CS;           // O columns per softmax thread
     static constexpr int DB = D / 64;             // 64-column (128-byte) swizzle blocks
@@ -135,6 +135,7 @@ struct FwdCfg {
     static_assert(D % 64 == 0 && D >= 64 && D <= 256, "D must be 64, 128 or 256");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64, 256]");
     static_assert(CS == 1 || CS == 2, "one or two warps per row");
+    static_assert(NS == 1 || NS == 2, "one or two S buffers per Q tile");
     static_assert(NCOL % 32 == 0 && OCOL % 32 == 0, "per-thread column slices are whole 32-column loads");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");

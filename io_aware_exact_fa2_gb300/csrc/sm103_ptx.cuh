@@ -44,9 +44,38 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// How a thread polls an mbarrier phase:
+//   0: try_wait (the hardware may suspend the thread until the phase completes
+//      or a system-defined time limit passes),
+//   1: test_wait (never suspends: a tight poll),
+//   2: try_wait with a short suspend-time hint (FA2_MBAR_SUSPEND_NS).
+#ifndef FA2_MBAR_WAIT_MODE
+#define FA2_MBAR_WAIT_MODE 0
+#endif
+#ifndef FA2_MBAR_SUSPEND_NS
+#define FA2_MBAR_SUSPEND_NS 20
+#endif
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
+#if FA2_MBAR_WAIT_MODE == 1
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+#elif FA2_MBAR_WAIT_MODE == 2
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(FA2_MBAR_SUSPEND_NS)
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -54,6 +83,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
         : "=r"(ok)
         : "r"(bar), "r"(parity)
         : "memory");
+#endif
     return ok != 0;
 }
 
