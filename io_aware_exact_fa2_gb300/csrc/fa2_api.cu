@@ -55,6 +55,24 @@ unsigned long long wait_limit_ns()
     return limit;
 }
 
+// Number of SMs of a device (looked up once per device).
+int sm_count(int dev)
+{
+    static std::mutex mu;
+    static int cache[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0)
+        return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < kMaxDevices)
+        cache[dev] = n;
+    return n;
+}
+
 // Device address of g_device_error for the current device (looked up once per device).
 int *device_error_ptr(int dev)
 {
@@ -137,7 +155,8 @@ fa2_status launch(const void *q, const void *k, const void *v, void *o, float *l
     a.stream = stream;
     a.encode = encode_fn();
     a.device = dev;
-    if (!a.err || !a.encode)
+    a.num_sms = sm_count(dev);
+    if (!a.err || !a.encode || a.num_sms <= 0)
         return FA2_ERR_CUDA;
     switch (D) {
     case 64: return launch_fwd_d64(a);

@@ -3,7 +3,7 @@
 // The method (Olowookere, "FlashAttention-2 from scratch with a custom Triton
 // kernel", sections "The core idea: making attention IO-aware" and "Running
 // max m_i and running normaliser"; "Chapter 08: Flash Attention -- blocked
-// attention", sections 1-5): a CTA owns NQ query tiles of 128 rows of one
+// attention", sections 1-5): a work unit is NQ query tiles of 128 rows of one
 // (batch, head); the tiles stay on chip while K/V tiles of BN rows stream
 // through shared memory; per row the kernel keeps a running max m, a running
 // normaliser l and an unnormalised accumulator O, rescales O and l when m
@@ -15,23 +15,25 @@
 //
 // GB300 mapping (the pages' kernels are Triton for A100/Ada; this is not a
 // translation of them):
-//   * TMA (cp.async.bulk.tensor, 128B swizzle) moves Q once and K/V per tile
-//     into a KS-stage shared-memory ring guarded by mbarriers.
+//   * Persistent CTAs (one per SM) walk a static list of work units; causal
+//     units are ordered heaviest first and dealt out in a snake so heavy and
+//     light units pair up.  All barrier phases run on across units, so the next
+//     unit's Q and K/V tiles stream in while the current unit finishes.
+//   * TMA (cp.async.bulk.tensor, 128B swizzle) moves Q (per unit) and K/V (per
+//     tile) into shared memory: a Q buffer per Q tile, refilled as soon as the
+//     last S MMA that reads it completes, and a KS-stage K/V ring.
 //   * One warp issues tcgen05.mma (a single elected lane, warp-uniform control
 //     flow, descriptors precomputed): S = Q K^T into TMEM (fp32), then
 //     O += P V with P read straight from TMEM (bf16, aliasing S) and V from
-//     shared memory as an MN-major operand (no transpose pass).  With one Q
-//     tile per CTA each tile has two S buffers, so S(j+1) is computed while
-//     the softmax of tile j runs.
+//     shared memory as an MN-major operand (no transpose pass).
 //   * Softmax: CS warps share each row (TMEM lane == row; warp w may touch
 //     lanes 32*(w%4)..+31), each owning BN/CS columns of S and D/CS columns
-//     of O.  The row max is exchanged through shared memory every tile; the
-//     warps write P back to TMEM and rescale O in TMEM only when a row's max
-//     grows by more than 2^8 (the stale max is kept otherwise, which is exact
-//     because l and LSE use the same max).
-//   * The epilogue multiplies by 1/l, packs bf16 into the (now free) Q tile
-//     in the swizzled layout and stores it with TMA (rows >= Lq are clipped
-//     by the tensor bounds); LSE goes out as coalesced fp32 stores.
+//     of O.  They write P back to TMEM and rescale O in TMEM only when a
+//     row's max grows by more than 2^8 (the stale max is kept otherwise, which
+//     is exact because l and LSE use the same max).
+//   * Epilogue: the softmax warps read O out of TMEM, release it to the MMA
+//     warp (the next unit's PV may then overwrite it), multiply by 1/l and
+//     store bf16 rows and the fp32 LSE straight to global memory.
 //   * Every wait between warps is on an mbarrier with a time bound; a wait
 //     that runs out records a code in a device error word and the CTA winds
 //     down, so no input can hang the GPU.
@@ -45,12 +47,14 @@
 namespace fa2 {
 
 struct FwdParams {
+    uint16_t *o;                // bf16 [B*H, Lq, D]
     float *lse;                 // fp32 [B*H, Lq]
     int *err;                   // device error word
     unsigned long long wait_limit_ns;
     int Lq, Lk;
     int BH;                     // B * H
     int n_qgroups;              // ceil(Lq / (NQ * 128))
+    int n_units;                // n_qgroups * BH
     int causal;
     float scale_log2;           // scale * log2(e), > 0
 };
@@ -71,7 +75,7 @@ template <int D_, int BN_, int NQ_, int KS_, int CS_, int NS_ = (NQ_ == 1 ? 2 : 
 struct FwdCfg {
     static constexpr int D = D_;     // head dimension
     static constexpr int BN = BN_;   // K/V rows per tile
-    static constexpr int NQ = NQ_;   // 128-row Q tiles per CTA
+    static constexpr int NQ = NQ_;   // 128-row Q tiles per work unit
     static constexpr int KS = KS_;   // K/V ring stages
     static constexpr int CS = CS_;   // softmax warps sharing one row (column split)
     static constexpr int BM = 128;   // Q rows per tile = TMEM lanes = MMA M
@@ -91,15 +95,17 @@ struct FwdCfg {
     static constexpr int OFF_XMAX = OFF_V + KS * KV_TILE;           // f32 [NQ][2][CS][128]
     static constexpr int OFF_XL = OFF_XMAX + NQ * 2 * CS * 128 * 4;  // f32x2 [NQ][CS][128]
     static constexpr int OFF_BAR = OFF_XL + NQ * CS * 128 * 8;
-    static constexpr int BAR_Q = 0;
-    static constexpr int BAR_K_FULL = 1;
+    static constexpr int BAR_Q_FULL = 0;                     // [NQ]
+    static constexpr int BAR_Q_EMPTY = BAR_Q_FULL + NQ;      // [NQ]
+    static constexpr int BAR_K_FULL = BAR_Q_EMPTY + NQ;      // [KS]
     static constexpr int BAR_K_EMPTY = BAR_K_FULL + KS;
     static constexpr int BAR_V_FULL = BAR_K_EMPTY + KS;
     static constexpr int BAR_V_EMPTY = BAR_V_FULL + KS;
     static constexpr int BAR_S_FULL = BAR_V_EMPTY + KS;      // [NQ][NS]
-    static constexpr int BAR_O_DONE = BAR_S_FULL + NQ * NS;  // [NQ]
-    static constexpr int BAR_P_READY = BAR_O_DONE + NQ;      // [NQ][NS]
-    static constexpr int BAR_XMAX = BAR_P_READY + NQ * NS;   // [NQ][2]
+    static constexpr int BAR_P_READY = BAR_S_FULL + NQ * NS; // [NQ][NS]
+    static constexpr int BAR_O_DONE = BAR_P_READY + NQ * NS; // [NQ]
+    static constexpr int BAR_O_FREE = BAR_O_DONE + NQ;       // [NQ]
+    static constexpr int BAR_XMAX = BAR_O_FREE + NQ;         // [NQ][2]
     static constexpr int BAR_GROUP = BAR_XMAX + 2 * NQ;      // [NQ]
     static constexpr int BAR_DRAIN = BAR_GROUP + NQ;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
@@ -121,10 +127,10 @@ struct FwdCfg {
     static constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;
     // With two softmax warpgroups the launch leaves 168 registers per thread; the
     // control warpgroup drops to REG_CTRL and the softmax warpgroups rise to
-    // REG_SOFTMAX.  Budget: 2*128*208 + 128*88 = 64512 = 384 threads * 168.
+    // REG_SOFTMAX.  Budget: 2*128*200 + 128*104 = 64512 = 384 threads * 168.
     static constexpr bool REG_SPLIT = (NUM_SOFTMAX_WARPS == 8);
-    static constexpr int REG_SOFTMAX = 208;
-    static constexpr int REG_CTRL = 88;
+    static constexpr int REG_SOFTMAX = 200;
+    static constexpr int REG_CTRL = 104;
     static constexpr int NUM_THREADS = 32 * (NUM_SOFTMAX_WARPS + (REG_SPLIT ? 4 : 2));
     static_assert(!REG_SPLIT || 2 * 128 * REG_SOFTMAX + 128 * REG_CTRL <= NUM_THREADS * 168,
                   "register split exceeds the launch allocation");
@@ -134,6 +140,7 @@ struct FwdCfg {
 
     static_assert(D % 64 == 0 && D >= 64 && D <= 256, "D must be 64, 128 or 256");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64, 256]");
+    static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per work unit");
     static_assert(CS == 1 || CS == 2, "one or two warps per row");
     static_assert(NS == 1 || NS == 2, "one or two S buffers per Q tile");
     static_assert(NCOL % 32 == 0 && OCOL % 32 == 0, "per-thread column slices are whole 32-column loads");
@@ -154,6 +161,30 @@ __device__ __forceinline__ int kv_tiles_for(int q0, int Lq, int Lk, int causal, 
     return last_key / BN + 1;
 }
 
+// The work unit a CTA handles at its i-th step, or -1 when it has no more.
+// Units are numbered heaviest first for causal (query groups from the bottom
+// of the score matrix up) and dealt to the CTAs in a snake, so a CTA that got
+// a heavy unit in one round gets a light one in the next.
+__device__ __forceinline__ int unit_at(int i, int n_units, int causal)
+{
+    const int g = static_cast<int>(gridDim.x);
+    const int k = static_cast<int>(blockIdx.x);
+    const int idx = i * g + ((causal && (i & 1)) ? (g - 1 - k) : k);
+    return idx < n_units ? idx : -1;
+}
+
+// unit -> (query group, batch*head)
+__device__ __forceinline__ void decode_unit(int idx, const FwdParams &p, int &qg, int &bh)
+{
+    if (p.causal) {
+        qg = p.n_qgroups - 1 - idx / p.BH;
+        bh = idx % p.BH;
+    } else {
+        bh = idx / p.n_qgroups;
+        qg = idx % p.n_qgroups;
+    }
+}
+
 // All lanes wait (bounded); the warp agrees on the outcome so warp-collective
 // tcgen05 instructions are executed by all lanes or by none.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *err, int code,
@@ -166,8 +197,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *er
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                   const FwdParams p)
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
 {
     using namespace ptx;
     extern __shared__ uint8_t smem_raw[];
@@ -175,37 +205,19 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work unit: (query group, batch*head).  Causal: heaviest groups first.
-    int qg, bh;
-    if (p.causal) {
-        qg = p.n_qgroups - 1 - static_cast<int>(blockIdx.x) / p.BH;
-        bh = static_cast<int>(blockIdx.x) % p.BH;
-    } else {
-        bh = static_cast<int>(blockIdx.x) / p.n_qgroups;
-        qg = static_cast<int>(blockIdx.x) % p.n_qgroups;
-    }
-    const int q0 = qg * (C::NQ * C::BM);
-    // K/V tiles visited by Q tile t (computed, not indexed, to keep it in registers)
-    auto n_of = [&](int t) { return kv_tiles_for(q0 + t * C::BM, p.Lq, p.Lk, p.causal, C::BN); };
-    int n_max = 0;
-#pragma unroll
-    for (int t = 0; t < C::NQ; ++t)
-        n_max = max(n_max, n_of(t));
-    // the last Q tile (highest t) that reads K/V tile j
-    auto last_user = [&](int j) {
-        int u = 0;
-#pragma unroll
-        for (int t = 0; t < C::NQ; ++t)
-            if (j < n_of(t))
-                u = t;
-        return u;
-    };
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
     // ---- setup: barriers, TMEM
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::BAR_Q), 1);
+        for (int t = 0; t < C::NQ; ++t) {
+            mbar_init(bar(C::BAR_Q_FULL + t), 1);
+            mbar_init(bar(C::BAR_Q_EMPTY + t), 1);
+            mbar_init(bar(C::BAR_O_DONE + t), 1);
+            mbar_init(bar(C::BAR_O_FREE + t), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_XMAX + 2 * t), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_XMAX + 2 * t + 1), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_GROUP + t), C::GROUP_THREADS);
+        }
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(bar(C::BAR_K_FULL + s), 1);
             mbar_init(bar(C::BAR_K_EMPTY + s), 1);
@@ -215,12 +227,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         for (int i = 0; i < C::NQ * C::NS; ++i) {
             mbar_init(bar(C::BAR_S_FULL + i), 1);
             mbar_init(bar(C::BAR_P_READY + i), C::GROUP_THREADS);
-        }
-        for (int t = 0; t < C::NQ; ++t) {
-            mbar_init(bar(C::BAR_O_DONE + t), 1);
-            mbar_init(bar(C::BAR_XMAX + 2 * t), C::GROUP_THREADS);
-            mbar_init(bar(C::BAR_XMAX + 2 * t + 1), C::GROUP_THREADS);
-            mbar_init(bar(C::BAR_GROUP + t), C::GROUP_THREADS);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
         fence_mbar_init();
@@ -245,132 +251,216 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_o);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            uint32_t q_bytes = 0;
+            uint32_t kv_iter = 0;            // K/V tiles issued so far (ring position)
+            uint32_t q_loads[C::NQ] = {};    // Q loads issued per Q buffer
+            bool k_pending = false;          // a K load of ring slot kv_iter is in flight without its V
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int u = unit_at(i, p.n_units, p.causal);
+                if (u < 0)
+                    break;
+                int qg, bh;
+                decode_unit(u, p, qg, bh);
+                const int q0 = qg * (C::NQ * C::BM);
+                int n_max = 0;
 #pragma unroll
-            for (int t = 0; t < C::NQ; ++t)
-                if (n_of(t) > 0)
-                    q_bytes += C::Q_TILE;
-            mbar_arrive_expect_tx(bar(C::BAR_Q), q_bytes);
+                for (int t = 0; t < C::NQ; ++t) {
+                    const int n = kv_tiles_for(q0 + t * C::BM, p.Lq, p.Lk, p.causal, C::BN);
+                    n_max = max(n_max, n);
+                    if (n > 0 && ok) {
+                        // the buffer is free once the last S MMA of the previous unit read it
+                        if (q_loads[t] > 0 &&
+                            !mbar_wait(bar(C::BAR_Q_EMPTY + t), (q_loads[t] - 1) & 1, p.err, ERR_PRODUCER | 3,
+                                       p.wait_limit_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(C::BAR_Q_FULL + t), C::Q_TILE);
 #pragma unroll
-            for (int t = 0; t < C::NQ; ++t)
-                if (n_of(t) > 0)
+                        for (int c = 0; c < C::DB; ++c)
+                            tma_load_3d_hint(sbase + C::OFF_Q + t * C::Q_TILE + c * C::Q_BLOCK, &tm_q, 64 * c,
+                                             q0 + t * C::BM, bh, bar(C::BAR_Q_FULL + t), pol_q);
+                        ++q_loads[t];
+                    }
+                }
+                for (int j = 0; j < n_max && ok; ++j, ++kv_iter) {
+                    const int s = kv_iter % C::KS;
+                    const uint32_t ph = (kv_iter / C::KS) & 1;
+                    if (!mbar_wait(bar(C::BAR_K_EMPTY + s), ph ^ 1u, p.err, ERR_PRODUCER | 1, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(C::BAR_K_FULL + s), C::KV_TILE);
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
-                        tma_load_3d_hint(sbase + C::OFF_Q + t * C::Q_TILE + c * C::Q_BLOCK, &tm_q, 64 * c,
-                                         q0 + t * C::BM, bh, bar(C::BAR_Q), pol_q);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n_max; ++j) {
-                const int s = j % C::KS;
-                const uint32_t ph = (j / C::KS) & 1;
-                if (!mbar_wait(bar(C::BAR_K_EMPTY + s), ph ^ 1u, p.err, ERR_PRODUCER | 1, p.wait_limit_ns))
-                    break;
-                mbar_arrive_expect_tx(bar(C::BAR_K_FULL + s), C::KV_TILE);
+                        tma_load_3d_hint(sbase + C::OFF_K + s * C::KV_TILE + c * C::KV_BLOCK, &tm_k, 64 * c,
+                                         j * C::BN, bh, bar(C::BAR_K_FULL + s), pol_kv);
+                    k_pending = true;
+                    if (!mbar_wait(bar(C::BAR_V_EMPTY + s), ph ^ 1u, p.err, ERR_PRODUCER | 2, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(C::BAR_V_FULL + s), C::KV_TILE);
 #pragma unroll
-                for (int c = 0; c < C::DB; ++c)
-                    tma_load_3d_hint(sbase + C::OFF_K + s * C::KV_TILE + c * C::KV_BLOCK, &tm_k, 64 * c,
-                                     j * C::BN, bh, bar(C::BAR_K_FULL + s), pol_kv);
-                k_issued = j + 1;
-                if (!mbar_wait(bar(C::BAR_V_EMPTY + s), ph ^ 1u, p.err, ERR_PRODUCER | 2, p.wait_limit_ns))
-                    break;
-                mbar_arrive_expect_tx(bar(C::BAR_V_FULL + s), C::KV_TILE);
-#pragma unroll
-                for (int c = 0; c < C::DB; ++c)
-                    tma_load_3d_hint(sbase + C::OFF_V + s * C::KV_TILE + c * C::KV_BLOCK, &tm_v, 64 * c,
-                                     j * C::BN, bh, bar(C::BAR_V_FULL + s), pol_kv);
-                v_issued = j + 1;
+                    for (int c = 0; c < C::DB; ++c)
+                        tma_load_3d_hint(sbase + C::OFF_V + s * C::KV_TILE + c * C::KV_BLOCK, &tm_v, 64 * c,
+                                         j * C::BN, bh, bar(C::BAR_V_FULL + s), pol_kv);
+                    k_pending = false;
+                }
             }
             // Before the CTA may exit, every load this thread started must have landed
-            // (immediate on the normal path: all of them were consumed).
-            mbar_wait(bar(C::BAR_Q), 0, p.err, ERR_DRAIN | 1, p.wait_limit_ns);
-            for (int j = max(0, k_issued - C::KS); j < k_issued; ++j)
-                mbar_wait(bar(C::BAR_K_FULL + j % C::KS), (j / C::KS) & 1, p.err, ERR_DRAIN | 2,
+            // (immediate on the normal path: all of them were consumed).  After an
+            // abort between a K and its V load, that K load is awaited too.
+#pragma unroll
+            for (int t = 0; t < C::NQ; ++t)
+                if (q_loads[t] > 0)
+                    mbar_wait(bar(C::BAR_Q_FULL + t), (q_loads[t] - 1) & 1, p.err, ERR_DRAIN | 1, p.wait_limit_ns);
+            const uint32_t k_done = kv_iter + (k_pending ? 1u : 0u);
+            for (uint32_t it = (k_done > C::KS ? k_done - C::KS : 0); it < k_done; ++it)
+                mbar_wait(bar(C::BAR_K_FULL + it % C::KS), (it / C::KS) & 1, p.err, ERR_DRAIN | 2,
                           p.wait_limit_ns);
-            for (int j = max(0, v_issued - C::KS); j < v_issued; ++j)
-                mbar_wait(bar(C::BAR_V_FULL + j % C::KS), (j / C::KS) & 1, p.err, ERR_DRAIN | 3,
+            for (uint32_t it = (kv_iter > C::KS ? kv_iter - C::KS : 0); it < kv_iter; ++it)
+                mbar_wait(bar(C::BAR_V_FULL + it % C::KS), (it / C::KS) & 1, p.err, ERR_DRAIN | 3,
                           p.wait_limit_ns);
         }
         __syncwarp();
-    } else if (warp == C::WARP_MMA) {
+      } else if (warp == C::WARP_MMA) {
         // ================================================== MMA issuer
         // The whole warp runs the (uniform) control flow and the waits; one
         // elected lane issues the MMAs and commits.
         const bool leader = elect_one();
-        bool ok = warp_wait(bar(C::BAR_Q), 0, p.err, ERR_MMA | 1, p.wait_limit_ns);
-        tc_fence_after();
         // Descriptor bases; a K step moves the start address, which is the low
         // field of the descriptor in 16-byte units, so it is a plain add.
         const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
         const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
         const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_V, C::KV_BLOCK, 1024);
+        uint32_t kv_iter = 0;              // ring position of the current unit's K/V tile 0
+        uint32_t tbase[C::NQ] = {};        // S/PV tiles of each Q buffer in earlier units
+        uint32_t q_loads[C::NQ] = {};      // Q loads consumed per Q buffer
+        uint32_t units[C::NQ] = {};        // earlier units that used each Q buffer
+        bool ok = true;
 
-        // S(t, j) = Q_t K_j^T  into S/P buffer (t, j % NS)
-        auto issue_s = [&](int t, int j) -> bool {
-            const int s = j % C::KS;
-            if (!warp_wait(bar(C::BAR_K_FULL + s), (j / C::KS) & 1, p.err, ERR_MMA | 2, p.wait_limit_ns))
-                return false;
-            tc_fence_after();
-            if (leader) {
-                const uint32_t d = tmem + C::TM_S + (t * C::NS + j % C::NS) * C::BN;
-                const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
-                const uint64_t dk = desc_k + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < C::D / 16; ++kk)
-                    mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
-                           dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
-                           C::IDESC_S, kk > 0 ? 1u : 0u);
-                mma_commit(bar(C::BAR_S_FULL + t * C::NS + j % C::NS));
-                if (last_user(j) == t)
-                    mma_commit(bar(C::BAR_K_EMPTY + s));
-            }
-            __syncwarp();
-            return true;
-        };
-        // O_t (+)= P(t, j) V_j, P read from TMEM
-        auto issue_pv = [&](int t, int j) -> bool {
-            const int s = j % C::KS;
-            if (!warp_wait(bar(C::BAR_P_READY + t * C::NS + j % C::NS), (j / C::NS) & 1, p.err, ERR_MMA | 3,
-                           p.wait_limit_ns))
-                return false;
-            if (!warp_wait(bar(C::BAR_V_FULL + s), (j / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
-                return false;
-            tc_fence_after();
-            if (leader) {
-                const uint32_t d = tmem + C::TM_O + t * C::D;
-                const uint32_t a = tmem + C::TM_S + (t * C::NS + j % C::NS) * C::BN;
-                const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
-                    mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(C::BAR_O_DONE + t));
-                if (last_user(j) == t)
-                    mma_commit(bar(C::BAR_V_EMPTY + s));
-            }
-            __syncwarp();
-            return true;
-        };
-
-        // Issue order: S for the first NS tiles of every Q tile, then per K/V
-        // tile j and Q tile t: PV(t, j) followed by S(t, j + NS), which reuses
-        // the TMEM buffer PV(t, j) just read (tcgen05 ops execute in order).
-#pragma unroll
-        for (int b = 0; b < C::NS; ++b)
-#pragma unroll
-            for (int t = 0; t < C::NQ; ++t)
-                if (ok && b < n_of(t))
-                    ok = issue_s(t, b);
-        for (int j = 0; j < n_max && ok; ++j) {
+        for (int i = 0; ok; ++i) {
+            const int u = unit_at(i, p.n_units, p.causal);
+            if (u < 0)
+                break;
+            int qg, bh;
+            decode_unit(u, p, qg, bh);
+            const int q0 = qg * (C::NQ * C::BM);
+            int n_t[C::NQ];
+            int n_max = 0;
 #pragma unroll
             for (int t = 0; t < C::NQ; ++t) {
-                if (ok && j < n_of(t)) {
-                    ok = issue_pv(t, j);
-                    if (ok && j + C::NS < n_of(t))
-                        ok = issue_s(t, j + C::NS);
+                n_t[t] = kv_tiles_for(q0 + t * C::BM, p.Lq, p.Lk, p.causal, C::BN);
+                n_max = max(n_max, n_t[t]);
+            }
+            // the last Q tile (highest t) that reads K/V tile j
+            auto last_user = [&](int j) {
+                int lu = 0;
+#pragma unroll
+                for (int t = 0; t < C::NQ; ++t)
+                    if (j < n_t[t])
+                        lu = t;
+                return lu;
+            };
+
+            // S(t, j) = Q_t K_j^T  into S/P buffer (t, (tbase + j) % NS)
+            auto issue_s = [&](int t, int j) -> bool {
+                const uint32_t it = kv_iter + j;
+                const int s = it % C::KS;
+                if (!warp_wait(bar(C::BAR_K_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 2, p.wait_limit_ns))
+                    return false;
+                tc_fence_after();
+                const uint32_t g = tbase[t] + j;
+                const int b = g % C::NS;
+                if (leader) {
+                    const uint32_t d = tmem + C::TM_S + (t * C::NS + b) * C::BN;
+                    const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
+                    const uint64_t dk = desc_k + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < C::D / 16; ++kk)
+                        mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
+                               dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
+                               C::IDESC_S, kk > 0 ? 1u : 0u);
+                    mma_commit(bar(C::BAR_S_FULL + t * C::NS + b));
+                    if (last_user(j) == t)
+                        mma_commit(bar(C::BAR_K_EMPTY + s));
+                    if (j == n_t[t] - 1)
+                        mma_commit(bar(C::BAR_Q_EMPTY + t));   // last read of this unit's Q tile
+                }
+                __syncwarp();
+                return true;
+            };
+            // O_t (+)= P(t, j) V_j, P read from TMEM
+            auto issue_pv = [&](int t, int j) -> bool {
+                const uint32_t it = kv_iter + j;
+                const int s = it % C::KS;
+                const uint32_t g = tbase[t] + j;
+                const int b = g % C::NS;
+                if (!warp_wait(bar(C::BAR_P_READY + t * C::NS + b), (g / C::NS) & 1, p.err, ERR_MMA | 3,
+                               p.wait_limit_ns))
+                    return false;
+                if (!warp_wait(bar(C::BAR_V_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
+                    return false;
+                // the first PV of a unit overwrites O_t: the previous unit's epilogue
+                // must have read it out of TMEM
+                if (j == 0 && units[t] > 0 &&
+                    !warp_wait(bar(C::BAR_O_FREE + t), (units[t] - 1) & 1, p.err, ERR_MMA | 5, p.wait_limit_ns))
+                    return false;
+                tc_fence_after();
+                if (leader) {
+                    const uint32_t d = tmem + C::TM_O + t * C::D;
+                    const uint32_t a = tmem + C::TM_S + (t * C::NS + b) * C::BN;
+                    const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; ++kk)
+                        mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(bar(C::BAR_O_DONE + t));
+                    if (last_user(j) == t)
+                        mma_commit(bar(C::BAR_V_EMPTY + s));
+                }
+                __syncwarp();
+                return true;
+            };
+
+            // this unit's Q tiles
+#pragma unroll
+            for (int t = 0; t < C::NQ; ++t) {
+                if (ok && n_t[t] > 0) {
+                    ok = warp_wait(bar(C::BAR_Q_FULL + t), q_loads[t] & 1, p.err, ERR_MMA | 1, p.wait_limit_ns);
+                    ++q_loads[t];
                 }
             }
+            // Issue order: S for the first NS tiles of every Q tile, then per K/V
+            // tile j and Q tile t: PV(t, j) followed by S(t, j + NS), which reuses
+            // the TMEM buffer PV(t, j) just read (tcgen05 ops execute in order).
+#pragma unroll
+            for (int b = 0; b < C::NS; ++b)
+#pragma unroll
+                for (int t = 0; t < C::NQ; ++t)
+                    if (ok && b < n_t[t])
+                        ok = issue_s(t, b);
+            for (int j = 0; j < n_max && ok; ++j) {
+#pragma unroll
+                for (int t = 0; t < C::NQ; ++t) {
+                    if (ok && j < n_t[t]) {
+                        ok = issue_pv(t, j);
+                        if (ok && j + C::NS < n_t[t])
+                            ok = issue_s(t, j + C::NS);
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < C::NQ; ++t) {
+                if (n_t[t] > 0) {
+                    tbase[t] += n_t[t];
+                    ++units[t];
+                }
+            }
+            kv_iter += n_max;
         }
         // drain: every MMA issued above has completed before TMEM can be released
         if (leader)
@@ -382,246 +472,249 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         // ================================================== softmax warps
         if constexpr (C::REG_SPLIT)
             setmaxnreg_inc<C::REG_SOFTMAX>();
-        const int t = warp / (4 * C::CS);        // Q tile
+        const int t = warp / (4 * C::CS);        // Q tile slot
         const int h = (warp >> 2) % C::CS;       // column slice
         const int quarter = warp & 3;            // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;
-        const int q0_t = q0 + t * C::BM;
-        const int grow = q0_t + row;             // query index
-        const int n = n_of(t);
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t o_addr = tmem + lane_base + C::TM_O + t * C::D + h * C::OCOL;
         const uint32_t xmax = sbase + C::OFF_XMAX + t * (2 * C::CS * 128 * 4);
+        const uint32_t xl = sbase + C::OFF_XL + t * (C::CS * 128 * 8);
         const float c2 = p.scale_log2;
-        float m_use = -INFINITY;   // running max (log2 domain, possibly stale by < 2^THRESHOLD)
-        float l = 0.f;             // running normaliser of the fp32 weights (for LSE)
-        float l_o = 0.f;           // running normaliser of the bf16 weights the PV MMA sees (for O)
+        uint32_t tbase = 0;    // S tiles of this slot in earlier units (running phase base)
+        uint32_t units = 0;    // earlier units of this slot
         bool ok = true;
 
-        for (int j = 0; j < n && ok; ++j) {
-            const int b = j % C::NS;
-            ok = warp_wait(bar(C::BAR_S_FULL + t * C::NS + b), (j / C::NS) & 1, p.err, ERR_SOFTMAX | 1,
-                           p.wait_limit_ns);
-            if (!ok)
+        for (int i = 0; ok; ++i) {
+            const int u = unit_at(i, p.n_units, p.causal);
+            if (u < 0)
                 break;
-            tc_fence_after();
-            const uint32_t s_addr = tmem + lane_base + C::TM_S + (t * C::NS + b) * C::BN;
+            int qg, bh;
+            decode_unit(u, p, qg, bh);
+            const int q0_t = qg * (C::NQ * C::BM) + t * C::BM;
+            const int grow = q0_t + row;             // query index
+            const int n = kv_tiles_for(q0_t, p.Lq, p.Lk, p.causal, C::BN);
+            if (n == 0)
+                continue;
+            float m_use = -INFINITY;   // running max (log2 domain, possibly stale by < 2^THRESHOLD)
+            float l = 0.f;             // running normaliser of the fp32 weights (for LSE)
+            float l_o = 0.f;           // running normaliser of the bf16 weights the PV MMA sees (for O)
 
-            float s[C::NCOL];
-            {
-                uint32_t r[C::NCOL / 32][32];
-#pragma unroll
-                for (int q = 0; q < C::NCOL / 32; ++q)
-                    tmem_ld32(s_addr + h * C::NCOL + 32 * q, r[q]);
-#pragma unroll
-                for (int q = 0; q < C::NCOL / 32; ++q)
-                    tmem_ld_wait(r[q]);
-#pragma unroll
-                for (int q = 0; q < C::NCOL / 32; ++q)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        s[32 * q + i] = __uint_as_float(r[q][i]);
-            }
-
-            // mask: key tail (j >= Lk) and, on tiles crossing the diagonal, causal j > i
-            const int k0 = j * C::BN + h * C::NCOL;
-            if ((p.causal && j * C::BN + C::BN - 1 > q0_t) || (j * C::BN + C::BN > p.Lk)) {
-                const int lim = p.causal ? min(grow + 1, p.Lk) : p.Lk;  // keys < lim are visible
-#pragma unroll
-                for (int c = 0; c < C::NCOL; ++c)
-                    if (k0 + c >= lim)
-                        s[c] = -INFINITY;
-            }
-
-            // row max of this tile (own slice, then the other slices through shared
-            // memory): four independent chains of 3-input maxima
-            float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-            for (int c = 4; c < C::NCOL; c += 8) {
-                mx0 = max3(mx0, s[c], s[c + 1]);
-                mx1 = max3(mx1, s[c + 2], s[c + 3]);
-                if (c + 4 < C::NCOL) {
-                    mx2 = max3(mx2, s[c + 4], s[c + 5]);
-                    mx3 = max3(mx3, s[c + 6], s[c + 7]);
-                }
-            }
-            float mx = fmaxf(max3(mx0, mx1, mx2), mx3);
-            if constexpr (C::CS > 1) {
-                const uint32_t xb = xmax + (j & 1) * (C::CS * 128 * 4);
-                st_shared_f32(xb + (h * 128 + row) * 4, mx);
-                mbar_arrive(bar(C::BAR_XMAX + 2 * t + (j & 1)));
-                ok = warp_wait(bar(C::BAR_XMAX + 2 * t + (j & 1)), (j >> 1) & 1, p.err, ERR_SOFTMAX | 4,
+            for (int j = 0; j < n && ok; ++j) {
+                const uint32_t g = tbase + j;
+                const int b = g % C::NS;
+                ok = warp_wait(bar(C::BAR_S_FULL + t * C::NS + b), (g / C::NS) & 1, p.err, ERR_SOFTMAX | 1,
                                p.wait_limit_ns);
                 if (!ok)
                     break;
-#pragma unroll
-                for (int hh = 0; hh < C::CS; ++hh)
-                    if (hh != h)
-                        mx = fmaxf(mx, ld_shared_f32(xb + (hh * 128 + row) * 4));
-            }
-            const float m_tile = mx * c2;
-
-            // The first tile always holds key 0, which every row may see, so m_tile is
-            // finite there; later tiles keep the stale max unless it grows a lot.  All
-            // slices of a row see the same m_tile and so take the same decision.
-            float alpha = 1.f;
-            bool rescale = false;
-            if (j == 0) {
-                m_use = m_tile;
-            } else if (m_tile > m_use + RESCALE_THRESHOLD) {
-                alpha = ex2_approx(m_use - m_tile);
-                m_use = m_tile;
-                rescale = true;
-            }
-
-            // p = 2^(s * scale * log2e - m); masked entries give 2^-inf = 0.  P goes to
-            // TMEM as bf16 (two per 32-bit column, over the first BN/2 columns of the S
-            // buffer; this slice's keys land in columns h*NCOL/2 ..).  Two normalisers
-            // are kept: l sums the fp32 p (LSE needs the exact sum) and l_o sums the
-            // bf16-rounded p that the PV MMA multiplies, so O's numerator and
-            // denominator use the same weights -- with one dominant key the rounding
-            // of its weight then cancels instead of showing up in O.
-            // (scale and subtract, and the exact sum, run as packed fp32 pairs)
-            const uint64_t c2x2 = f32x2(c2, c2);
-            const uint64_t negm2 = f32x2(-m_use, -m_use);
-            uint64_t ls01 = 0, ls23 = 0;   // packed (0.f, 0.f)
-            float lr0 = 0.f, lr1 = 0.f;
-            {
-                uint32_t pk[C::NCOL / 2];
-#pragma unroll
-                for (int c = 0; c < C::NCOL; c += 4) {
-                    float x0, x1, x2, x3;
-                    unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), c2x2, negm2), x0, x1);
-                    unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), c2x2, negm2), x2, x3);
-                    const float p0 = ex2_approx(x0);
-                    const float p1 = ex2_approx(x1);
-                    const float p2 = ex2_approx(x2);
-                    const float p3 = ex2_approx(x3);
-                    const uint32_t w0 = pack_bf16x2(p0, p1);
-                    const uint32_t w1 = pack_bf16x2(p2, p3);
-                    pk[c / 2] = w0;
-                    pk[c / 2 + 1] = w1;
-                    ls01 = add_f32x2(ls01, f32x2(p0, p1));
-                    ls23 = add_f32x2(ls23, f32x2(p2, p3));
-                    lr0 = add_bf16x2_to_f32(lr0, w0);
-                    lr1 = add_bf16x2_to_f32(lr1, w1);
-                }
-                const uint32_t p_addr = s_addr + h * (C::NCOL / 2);
-                if constexpr (C::NCOL / 2 >= 32) {
-#pragma unroll
-                    for (int q = 0; q < C::NCOL / 64; ++q)
-                        tmem_st32(p_addr + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * q));
-                } else {
-                    tmem_st16(p_addr, pk);
-                }
-            }
-            {
-                float a0, a1, a2, a3;
-                unpack_f32x2(ls01, a0, a1);
-                unpack_f32x2(ls23, a2, a3);
-                l = l * alpha + ((a0 + a1) + (a2 + a3));
-            }
-            l_o = l_o * alpha + (lr0 + lr1);
-
-            // Rescale this slice of O (only warps in which some row's max grew) once
-            // the previous PV has landed.  Without a rescale there is nothing to wait
-            // for: the MMA warp orders PV(j) after PV(j-1) by itself.  A parity wait on
-            // O_DONE is only unambiguous while that barrier is at most one phase behind
-            // the awaited one: here S(j) completing implies PV(j - NS) completed, so
-            // waiting for PV(j-1) is safe; and the wait at the last tile (taken even
-            // without a rescale) keeps the epilogue's wait for PV(n-1) safe too.
-            const bool grow_any = __any_sync(0xffffffffu, rescale);
-            if (j > 0 && (grow_any || j == n - 1)) {
-                ok = warp_wait(bar(C::BAR_O_DONE + t), (j - 1) & 1, p.err, ERR_SOFTMAX | 2, p.wait_limit_ns);
-                if (!ok)
-                    break;
                 tc_fence_after();
-                if (grow_any) {
-#pragma unroll 1
-                    for (int cc = 0; cc < C::OCOL / 32; ++cc) {
-                        uint32_t r[32];
-                        tmem_ld32(o_addr + 32 * cc, r);
-                        tmem_ld_wait(r);
+                const uint32_t s_addr = tmem + lane_base + C::TM_S + (t * C::NS + b) * C::BN;
+
+                float s[C::NCOL];
+                {
+                    uint32_t r[C::NCOL / 32][32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_addr + 32 * cc, r);
+                    for (int q = 0; q < C::NCOL / 32; ++q)
+                        tmem_ld32(s_addr + h * C::NCOL + 32 * q, r[q]);
+#pragma unroll
+                    for (int q = 0; q < C::NCOL / 32; ++q)
+                        tmem_ld_wait(r[q]);
+#pragma unroll
+                    for (int q = 0; q < C::NCOL / 32; ++q)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            s[32 * q + e] = __uint_as_float(r[q][e]);
+                }
+
+                // mask: key tail (j >= Lk) and, on tiles crossing the diagonal, causal j > i
+                const int k0 = j * C::BN + h * C::NCOL;
+                if ((p.causal && j * C::BN + C::BN - 1 > q0_t) || (j * C::BN + C::BN > p.Lk)) {
+                    const int lim = p.causal ? min(grow + 1, p.Lk) : p.Lk;  // keys < lim are visible
+#pragma unroll
+                    for (int c = 0; c < C::NCOL; ++c)
+                        if (k0 + c >= lim)
+                            s[c] = -INFINITY;
+                }
+
+                // row max of this tile (own slice, then the other slices through shared
+                // memory): four independent chains of 3-input maxima
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < C::NCOL; c += 8) {
+                    mx0 = max3(mx0, s[c], s[c + 1]);
+                    mx1 = max3(mx1, s[c + 2], s[c + 3]);
+                    if (c + 4 < C::NCOL) {
+                        mx2 = max3(mx2, s[c + 4], s[c + 5]);
+                        mx3 = max3(mx3, s[c + 6], s[c + 7]);
                     }
                 }
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            // P_READY is per S buffer: the softmax may finish tile j+1 before the MMA
-            // warp has seen tile j, but it can only reuse a buffer after the MMA warp
-            // issued the S that refills it, i.e. after it consumed that buffer's P.
-            mbar_arrive(bar(C::BAR_P_READY + t * C::NS + b));
-        }
-
-        // ---- epilogue: O / l -> bf16 -> swizzled smem (the Q tile) -> TMA store; LSE
-        if (ok && n > 0) {
-            ok = warp_wait(bar(C::BAR_O_DONE + t), (n - 1) & 1, p.err, ERR_SOFTMAX | 3, p.wait_limit_ns);
-            float l_tot = l, lo_tot = l_o;
-            const uint32_t xl = sbase + C::OFF_XL + t * (C::CS * 128 * 8);
-            if constexpr (C::CS > 1) {
-                if (ok) {
-                    st_shared_f32(xl + (h * 128 + row) * 8, l);
-                    st_shared_f32(xl + (h * 128 + row) * 8 + 4, l_o);
-                    mbar_arrive(bar(C::BAR_GROUP + t));
-                    ok = warp_wait(bar(C::BAR_GROUP + t), 0, p.err, ERR_SOFTMAX | 5, p.wait_limit_ns);
-                    if (ok) {
-                        l_tot = 0.f;
-                        lo_tot = 0.f;
+                float mx = fmaxf(max3(mx0, mx1, mx2), mx3);
+                if constexpr (C::CS > 1) {
+                    const uint32_t xb = xmax + (g & 1) * (C::CS * 128 * 4);
+                    st_shared_f32(xb + (h * 128 + row) * 4, mx);
+                    mbar_arrive(bar(C::BAR_XMAX + 2 * t + (g & 1)));
+                    ok = warp_wait(bar(C::BAR_XMAX + 2 * t + (g & 1)), (g >> 1) & 1, p.err, ERR_SOFTMAX | 4,
+                                   p.wait_limit_ns);
+                    if (!ok)
+                        break;
 #pragma unroll
-                        for (int hh = 0; hh < C::CS; ++hh) {
-                            l_tot += ld_shared_f32(xl + (hh * 128 + row) * 8);
-                            lo_tot += ld_shared_f32(xl + (hh * 128 + row) * 8 + 4);
+                    for (int hh = 0; hh < C::CS; ++hh)
+                        if (hh != h)
+                            mx = fmaxf(mx, ld_shared_f32(xb + (hh * 128 + row) * 4));
+                }
+                const float m_tile = mx * c2;
+
+                // The first tile always holds key 0, which every row may see, so m_tile is
+                // finite there; later tiles keep the stale max unless it grows a lot.  All
+                // slices of a row see the same m_tile and so take the same decision.
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m_use = m_tile;
+                } else if (m_tile > m_use + RESCALE_THRESHOLD) {
+                    alpha = ex2_approx(m_use - m_tile);
+                    m_use = m_tile;
+                    rescale = true;
+                }
+
+                // p = 2^(s * scale * log2e - m); masked entries give 2^-inf = 0.  P goes to
+                // TMEM as bf16 (two per 32-bit column, over the first BN/2 columns of the S
+                // buffer; this slice's keys land in columns h*NCOL/2 ..).  Two normalisers
+                // are kept: l sums the fp32 p (LSE needs the exact sum) and l_o sums the
+                // bf16-rounded p that the PV MMA multiplies, so O's numerator and
+                // denominator use the same weights -- with one dominant key the rounding
+                // of its weight then cancels instead of showing up in O.
+                // (scale and subtract, and the exact sum, run as packed fp32 pairs)
+                const uint64_t c2x2 = f32x2(c2, c2);
+                const uint64_t negm2 = f32x2(-m_use, -m_use);
+                uint64_t ls01 = 0, ls23 = 0;   // packed (0.f, 0.f)
+                float lr0 = 0.f, lr1 = 0.f;
+                {
+                    uint32_t pk[C::NCOL / 2];
+#pragma unroll
+                    for (int c = 0; c < C::NCOL; c += 4) {
+                        float x0, x1, x2, x3;
+                        unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), c2x2, negm2), x0, x1);
+                        unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), c2x2, negm2), x2, x3);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        const float p2 = ex2_approx(x2);
+                        const float p3 = ex2_approx(x3);
+                        const uint32_t w0 = pack_bf16x2(p0, p1);
+                        const uint32_t w1 = pack_bf16x2(p2, p3);
+                        pk[c / 2] = w0;
+                        pk[c / 2 + 1] = w1;
+                        ls01 = add_f32x2(ls01, f32x2(p0, p1));
+                        ls23 = add_f32x2(ls23, f32x2(p2, p3));
+                        lr0 = add_bf16x2_to_f32(lr0, w0);
+                        lr1 = add_bf16x2_to_f32(lr1, w1);
+                    }
+                    const uint32_t p_addr = s_addr + h * (C::NCOL / 2);
+                    if constexpr (C::NCOL / 2 >= 32) {
+#pragma unroll
+                        for (int q = 0; q < C::NCOL / 64; ++q)
+                            tmem_st32(p_addr + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * q));
+                    } else {
+                        tmem_st16(p_addr, pk);
+                    }
+                }
+                {
+                    float a0, a1, a2, a3;
+                    unpack_f32x2(ls01, a0, a1);
+                    unpack_f32x2(ls23, a2, a3);
+                    l = l * alpha + ((a0 + a1) + (a2 + a3));
+                }
+                l_o = l_o * alpha + (lr0 + lr1);
+
+                // Rescale this slice of O (only warps in which some row's max grew) once
+                // the previous PV has landed.  Without a rescale there is nothing to wait
+                // for: the MMA warp orders PV(j) after PV(j-1) by itself.  A parity wait on
+                // O_DONE is only unambiguous while that barrier is at most one phase behind
+                // the awaited one: here S(j) completing implies PV(j - NS) completed (and
+                // every earlier unit's PVs completed before its epilogue), so waiting for
+                // PV(j-1) is safe; the wait at the last tile (taken even without a rescale)
+                // keeps the epilogue's wait for PV(n-1) safe too.
+                const bool grow_any = __any_sync(0xffffffffu, rescale);
+                if (j > 0 && (grow_any || j == n - 1)) {
+                    ok = warp_wait(bar(C::BAR_O_DONE + t), (g - 1) & 1, p.err, ERR_SOFTMAX | 2, p.wait_limit_ns);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    if (grow_any) {
+#pragma unroll 1
+                        for (int cc = 0; cc < C::OCOL / 32; ++cc) {
+                            uint32_t r[32];
+                            tmem_ld32(o_addr + 32 * cc, r);
+                            tmem_ld_wait(r);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                            tmem_st32(o_addr + 32 * cc, r);
                         }
                     }
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                // P_READY is per S buffer: the softmax may finish tile j+1 before the MMA
+                // warp has seen tile j, but it can only reuse a buffer after the MMA warp
+                // issued the S that refills it, i.e. after it consumed that buffer's P.
+                mbar_arrive(bar(C::BAR_P_READY + t * C::NS + b));
             }
-            if (ok) {
-                tc_fence_after();
-                const float inv_l = 1.f / lo_tot;
-                const float lse = (m_use + lg2_approx(l_tot)) * LN2;
-                const uint32_t stage = sbase + C::OFF_Q + t * C::Q_TILE;
-#pragma unroll 1
-                for (int cc = 0; cc < C::OCOL / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + 32 * cc, r);
-                    tmem_ld_wait(r);
-                    uint32_t w[16];
+            if (!ok)
+                break;
+
+            // ---- epilogue: O out of TMEM (then released to the MMA warp), O / l -> bf16
+            // rows and LSE straight to global memory
+            const uint32_t g_last = tbase + n - 1;
+            ok = warp_wait(bar(C::BAR_O_DONE + t), g_last & 1, p.err, ERR_SOFTMAX | 3, p.wait_limit_ns);
+            if (!ok)
+                break;
+            float l_tot = l, lo_tot = l_o;
+            if constexpr (C::CS > 1) {
+                st_shared_f32(xl + (h * 128 + row) * 8, l);
+                st_shared_f32(xl + (h * 128 + row) * 8 + 4, l_o);
+                mbar_arrive(bar(C::BAR_GROUP + t));
+                ok = warp_wait(bar(C::BAR_GROUP + t), units & 1, p.err, ERR_SOFTMAX | 5, p.wait_limit_ns);
+                if (!ok)
+                    break;
+                l_tot = 0.f;
+                lo_tot = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-                    const int col0 = h * C::OCOL + 32 * cc;  // first O column of this chunk
-                    const uint32_t row_addr = stage + (col0 >> 6) * C::Q_BLOCK + row * 128;
-                    const int chunk0 = (col0 & 63) >> 3;     // first 16-byte chunk within the 128-byte row
+                for (int hh = 0; hh < C::CS; ++hh) {
+                    l_tot += ld_shared_f32(xl + (hh * 128 + row) * 8);
+                    lo_tot += ld_shared_f32(xl + (hh * 128 + row) * 8 + 4);
+                }
+            }
+            tc_fence_after();
+            const float inv_l = 1.f / lo_tot;
+            const float lse = (m_use + lg2_approx(l_tot)) * LN2;
+            const bool live = grow < p.Lq;
+            uint16_t *orow = p.o + (static_cast<size_t>(bh) * p.Lq + (live ? grow : 0)) * C::D + h * C::OCOL;
+#pragma unroll 1
+            for (int cc = 0; cc < C::OCOL / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(o_addr + 32 * cc, r);
+                tmem_ld_wait(r);
+                if (cc == C::OCOL / 32 - 1) {
+                    // every read of O_t is done: the next unit's first PV may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(bar(C::BAR_O_FREE + t));
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+                if (live) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        st_shared_v4(row_addr + (((chunk0 + q) ^ (row & 7)) << 4), w[4 * q], w[4 * q + 1],
-                                     w[4 * q + 2], w[4 * q + 3]);
+                        dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
                 }
-                fence_proxy_async_smem();
-                if constexpr (C::CS > 1) {
-                    mbar_arrive(bar(C::BAR_GROUP + t));
-                    if (h == 0)
-                        ok = warp_wait(bar(C::BAR_GROUP + t), 1, p.err, ERR_SOFTMAX | 6, p.wait_limit_ns);
-                } else {
-                    __syncwarp();
-                }
-                // the slice-0 warp of each lane quarter stores the quarter's 32 rows
-                const int r0 = q0_t + quarter * 32;
-                if (ok && h == 0 && lane == 0 && r0 < p.Lq) {
-#pragma unroll
-                    for (int c = 0; c < C::DB; ++c)
-                        tma_store_3d(&tm_o, 64 * c, r0, bh, stage + c * C::Q_BLOCK + quarter * 32 * 128);
-                    tma_store_commit();
-                    tma_store_wait_read_all();
-                }
-                __syncwarp();
-                if (ok && h == 0 && grow < p.Lq)
-                    p.lse[static_cast<size_t>(bh) * p.Lq + grow] = lse;
             }
+            if (h == 0 && live)
+                p.lse[static_cast<size_t>(bh) * p.Lq + grow] = lse;
+            tbase += n;
+            ++units;
         }
     }
 

@@ -28,11 +28,12 @@ struct LaunchArgs {
     cudaStream_t stream;
     EncodeTiledFn encode;
     int device;
+    int num_sms;    // streaming multiprocessors of `device`
 };
 
 // 3-D view of a contiguous bf16 [B*H, L, D] tensor: dims (D, L, B*H) innermost
 // first, a box of 64 columns (128 bytes, one swizzle span) by box_rows rows by
-// one head.  Rows outside [0, L) of a head read as zero and are never written.
+// one head.  Rows outside [0, L) of a head read as zero.
 inline bool encode_bhld(EncodeTiledFn encode, CUtensorMap *m, const void *ptr, int D, int L, int BH,
                         int box_rows)
 {
@@ -52,14 +53,14 @@ template <class C>
 fa2_status launch_fwd(const LaunchArgs &a)
 {
     const int BH = a.B * a.H;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (!encode_bhld(a.encode, &tq, a.q, C::D, a.Lq, BH, C::BM) ||
         !encode_bhld(a.encode, &tk, a.k, C::D, a.Lk, BH, C::BN) ||
-        !encode_bhld(a.encode, &tv, a.v, C::D, a.Lk, BH, C::BN) ||
-        !encode_bhld(a.encode, &to, a.o, C::D, a.Lq, BH, 32))
+        !encode_bhld(a.encode, &tv, a.v, C::D, a.Lk, BH, C::BN))
         return FA2_ERR_CUDA;
 
     FwdParams p;
+    p.o = static_cast<uint16_t *>(a.o);
     p.lse = a.lse;
     p.err = a.err;
     p.wait_limit_ns = a.wait_limit_ns;
@@ -69,9 +70,12 @@ fa2_status launch_fwd(const LaunchArgs &a)
     p.n_qgroups = (a.Lq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
     p.causal = a.causal ? 1 : 0;
     p.scale_log2 = a.scale_log2;
-    const long long grid = static_cast<long long>(p.n_qgroups) * BH;
-    if (grid > INT_MAX)
+    const long long units = static_cast<long long>(p.n_qgroups) * BH;
+    if (units > INT_MAX)
         return FA2_ERR_INVALID_ARG;
+    p.n_units = static_cast<int>(units);
+    // persistent grid: one CTA per SM (each holds all of TMEM), walking the units
+    const long long grid = units < a.num_sms ? units : a.num_sms;
 
     // opt in to more than 48 KB of dynamic shared memory, once per device
     static std::atomic<unsigned long long> configured{0};
@@ -84,8 +88,7 @@ fa2_status launch_fwd(const LaunchArgs &a)
         }
         configured.fetch_or(bit);
     }
-    fa2_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv,
-                                                                                               to, p);
+    fa2_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 

@@ -66,6 +66,14 @@ def test_many_heads_small_seq(D):
     check(3, 5, 130, 190, D, False, seed=600 + D)
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+def test_many_units_per_cta(D, causal):
+    """More work units than SMs, with ragged Lq/Lk, so each persistent CTA walks several
+    units (phases carried across units, Q/K/V prefetched for the next unit)."""
+    check(8, 20, 300, 457, D, causal, seed=650 + D)
+
+
 def test_lq_zero_is_a_noop():
     """Lq == 0: FA2_OK and nothing is written."""
     from io_aware_exact_fa2_gb300 import _binding
