@@ -37,6 +37,8 @@
 #ifndef FA2_GB300_H
 #define FA2_GB300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -70,6 +72,56 @@ typedef enum fa2_status {
 fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o,
                    float *lse, int B, int H, int Lq, int Lk, int D,
                    int causal, float scale, void *stream);
+
+/*
+ * fa2_workspace_size -- bytes of device workspace fa2_fwd_ws needs for this
+ * problem on `device` (its SM count sets the schedule).  *bytes = 0 when the
+ * pass uses none: causal passes, Lq == 0, and non-causal shapes for which
+ * dealing out whole query tiles already keeps the SMs evenly busy (the cut
+ * ranges are only used when they are estimated to save at least 5 %).  The
+ * environment variable FA2_SPLIT=always (or =never) overrides that estimate
+ * for this call and for the fa2_fwd_ws calls that follow; it must not change
+ * between sizing a workspace and the calls that use it.
+ *
+ *   B .. causal  as for fa2_fwd.
+ *   device       CUDA device ordinal the pass will run on.
+ *   bytes        out: required size in bytes.
+ *
+ * Returns FA2_OK; FA2_ERR_INVALID_ARG / FA2_ERR_UNSUPPORTED as fa2_fwd;
+ * FA2_ERR_CUDA if the device cannot be queried.
+ */
+fa2_status fa2_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
+                              int device, size_t *bytes);
+
+/*
+ * fa2_fwd_ws -- fa2_fwd with a caller-owned device workspace, which lets a
+ * non-causal pass balance the work evenly over the SMs: the key-tile
+ * iterations of all query tiles are cut into one equal range per SM, and a
+ * query tile whose keys straddle two ranges is computed in parts that are
+ * merged afterwards: each part's O and log-sum-exp are combined exactly as
+ * the online softmax merges two key blocks (Olowookere, "FlashAttention-2
+ * from scratch with a custom Triton kernel", section "Running max m_i and
+ * running normaliser"; "Chapter 08: Flash Attention -- blocked attention",
+ * section 2).  Causal passes ignore the workspace (they balance whole tiles,
+ * heaviest first).
+ *
+ *   workspace        device pointer, 256-byte aligned, at least
+ *                    fa2_workspace_size() bytes, ZERO-FILLED before its first
+ *                    use; every completed call leaves it ready for the next
+ *                    (the arrival counters at its start, the only part that
+ *                    must start at zero, are zero again).
+ *   workspace_bytes  its size.
+ *   (other arguments as for fa2_fwd)
+ *
+ * A NULL workspace (allowed when fa2_workspace_size reports 0) runs the pass
+ * as fa2_fwd does.  Calls that may run at the same time (different streams)
+ * must not share a workspace.  Errors: as fa2_fwd, plus FA2_ERR_INVALID_ARG
+ * for a misaligned workspace or one smaller than the pass needs.
+ */
+fa2_status fa2_fwd_ws(const void *q, const void *k, const void *v, void *o,
+                      float *lse, int B, int H, int Lq, int Lk, int D,
+                      int causal, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /*
  * fa2_fwd_from_host -- the same pass starting from, and ending in, HOST

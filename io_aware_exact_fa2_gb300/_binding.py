@@ -37,6 +37,10 @@ def load_library() -> ctypes.CDLL:
     lib.fa2_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa2_fwd_from_host.restype = i
     lib.fa2_fwd_from_host.argtypes = [vp] * 10 + [i, i, i, i, i, i, f, vp]
+    lib.fa2_workspace_size.restype = i
+    lib.fa2_workspace_size.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa2_fwd_ws.restype = i
+    lib.fa2_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa2_get_device_error.restype = i
     lib.fa2_get_device_error.argtypes = [vp, ctypes.POINTER(i)]
     lib.fa2_status_string.restype = ctypes.c_char_p
@@ -74,18 +78,50 @@ def _check_shapes(q, k, v, o, lse):
     return B, H, Lq, k.shape[2], D
 
 
-def fa2_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:
-    """Forward pass on CUDA tensors: writes o (bf16) and lse (fp32, natural log)."""
+def fa2_workspace_size(B: int, H: int, Lq: int, Lk: int, D: int, causal: bool, device: int = 0) -> int:
+    """Bytes of workspace fa2_fwd_ws needs on `device` (0 when the pass uses none)."""
+    n = ctypes.c_size_t(0)
+    st = _lib.fa2_workspace_size(B, H, Lq, Lk, D, int(bool(causal)), int(device), ctypes.byref(n))
+    if st != 0:
+        raise Fa2Error(st, "fa2_workspace_size")
+    return int(n.value)
+
+
+def fa2_workspace(q, k, causal: bool):
+    """A zero-filled uint8 CUDA tensor sized for fa2_fwd_ws on q's problem (None if not needed)."""
+    import torch
+    B, H, Lq, D = q.shape
+    n = fa2_workspace_size(B, H, Lq, k.shape[2], D, causal, q.device.index or 0)
+    return torch.zeros(n, dtype=torch.uint8, device=q.device) if n else None
+
+
+def fa2_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None,
+            workspace=None) -> None:
+    """Forward pass on CUDA tensors: writes o (bf16) and lse (fp32, natural log).
+
+    With `workspace` (from fa2_workspace) a non-causal pass balances its key
+    tiles evenly over the SMs (fa2_fwd_ws); without it, whole query tiles are
+    scheduled (fa2_fwd).
+    """
     B, H, Lq, Lk, D = _check_shapes(q, k, v, o, lse)
     for t in (q, k, v, o, lse):
         if not t.is_cuda or t.device != q.device:
             raise ValueError("all tensors must be on the same CUDA device")
     if scale is None:
         scale = D ** -0.5
-    st = _lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                      B, H, Lq, Lk, D, int(bool(causal)), float(scale), _stream_handle(stream, q.device))
+    if workspace is None:
+        st = _lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, Lq, Lk, D, int(bool(causal)), float(scale), _stream_handle(stream, q.device))
+        where = "fa2_fwd"
+    else:
+        if not workspace.is_cuda or workspace.device != q.device:
+            raise ValueError("workspace must be on q's CUDA device")
+        st = _lib.fa2_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             B, H, Lq, Lk, D, int(bool(causal)), float(scale), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+        where = "fa2_fwd_ws"
     if st != 0:
-        raise Fa2Error(st, "fa2_fwd")
+        raise Fa2Error(st, where)
 
 
 def fa2_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,

@@ -50,6 +50,21 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+def kernel_digest() -> str:
+    """Hash of the sources that decide what the forward kernel does on the device: the
+    kernel template, its PTX wrappers, the launch logic and the per-D instantiations (not
+    the C ABI wrapper or the header), so that recorded profiler counters stay valid
+    across host-only changes."""
+    h = hashlib.sha256()
+    files = sorted(f for f in os.listdir(CSRC)
+                   if f in ("fa2_fwd_kernel.cuh", "sm103_ptx.cuh", "fa2_launch.cuh")
+                   or (f.startswith("fa2_fwd_d") and f.endswith(".cu")))
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
 def _stamp_path() -> str:
     return os.path.join(BUILD, "digest.txt")
 

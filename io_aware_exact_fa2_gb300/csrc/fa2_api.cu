@@ -55,6 +55,19 @@ unsigned long long wait_limit_ns()
     return limit;
 }
 
+// Whether non-causal passes given a workspace cut their key-tile iterations
+// into equal per-SM ranges: FA2_SPLIT=always / never overrides the cost model
+// (read on every call, so a process can switch it between calls).
+int split_policy()
+{
+    const char *s = std::getenv("FA2_SPLIT");
+    if (s && std::strcmp(s, "always") == 0)
+        return SPLIT_ALWAYS;
+    if (s && std::strcmp(s, "never") == 0)
+        return SPLIT_NEVER;
+    return SPLIT_AUTO;
+}
+
 // Number of SMs of a device (looked up once per device).
 int sm_count(int dev)
 {
@@ -132,7 +145,8 @@ fa2_status select_device_of(const void *ptr, int *dev_out)
 }
 
 fa2_status launch(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Lq,
-                  int Lk, int D, int causal, float scale, cudaStream_t stream)
+                  int Lk, int D, int causal, float scale, cudaStream_t stream, void *workspace = nullptr,
+                  size_t workspace_bytes = 0)
 {
     int dev = 0;
     fa2_status st = select_device_of(q, &dev);
@@ -156,6 +170,9 @@ fa2_status launch(const void *q, const void *k, const void *v, void *o, float *l
     a.encode = encode_fn();
     a.device = dev;
     a.num_sms = sm_count(dev);
+    a.split_policy = split_policy();
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
     if (!a.err || !a.encode || a.num_sms <= 0)
         return FA2_ERR_CUDA;
     switch (D) {
@@ -166,8 +183,54 @@ fa2_status launch(const void *q, const void *k, const void *v, void *o, float *l
     }
 }
 
+size_t workspace_bytes(int B, int H, int Lq, int Lk, int D, int causal, int num_sms)
+{
+    switch (D) {
+    case 64: return workspace_bytes_d64(B, H, Lq, Lk, causal, num_sms, split_policy());
+    case 128: return workspace_bytes_d128(B, H, Lq, Lk, causal, num_sms, split_policy());
+    case 256: return workspace_bytes_d256(B, H, Lq, Lk, causal, num_sms, split_policy());
+    default: return 0;
+    }
+}
+
 }  // namespace
 }  // namespace fa2
+
+FA2_EXPORT fa2_status fa2_workspace_size(int B, int H, int Lq, int Lk, int D, int causal, int device,
+                                         size_t *bytes)
+{
+    if (!bytes)
+        return FA2_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (B <= 0 || H <= 0 || Lq < 0 || Lk <= 0 || D <= 0 || device < 0)
+        return FA2_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H > INT_MAX)
+        return FA2_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256)
+        return FA2_ERR_UNSUPPORTED;
+    if (causal || Lq == 0)
+        return FA2_OK;
+    const int sms = fa2::sm_count(device);
+    if (sms <= 0)
+        return FA2_ERR_CUDA;
+    *bytes = fa2::workspace_bytes(B, H, Lq, Lk, D, causal, sms);
+    return FA2_OK;
+}
+
+FA2_EXPORT fa2_status fa2_fwd_ws(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                                 int Lq, int Lk, int D, int causal, float scale, void *workspace,
+                                 size_t workspace_bytes, void *stream)
+{
+    fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
+    if (st != FA2_OK || Lq == 0)
+        return st;
+    if (causal)   // the causal pass balances whole units and needs no workspace
+        return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, static_cast<cudaStream_t>(stream));
+    if (workspace && !fa2::aligned(workspace, 256))
+        return FA2_ERR_INVALID_ARG;
+    return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, static_cast<cudaStream_t>(stream),
+                       workspace, workspace_bytes);
+}
 
 FA2_EXPORT fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                               int Lq, int Lk, int D, int causal, float scale, void *stream)

@@ -27,9 +27,13 @@ namespace fa2 {
 #define FA2_D128_CS 1
 #endif
 
-fa2_status launch_fwd_d128(const LaunchArgs &a)
+using CfgD128 = FwdCfg<128, FA2_D128_BN, FA2_D128_NQ, FA2_D128_KS, FA2_D128_CS, FA2_D128_NS>;
+
+fa2_status launch_fwd_d128(const LaunchArgs &a) { return launch_fwd<CfgD128>(a); }
+
+size_t workspace_bytes_d128(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy)
 {
-    return launch_fwd<FwdCfg<128, FA2_D128_BN, FA2_D128_NQ, FA2_D128_KS, FA2_D128_CS, FA2_D128_NS>>(a);
+    return workspace_bytes_for<CfgD128>(B, H, Lq, Lk, causal, num_sms, policy);
 }
 
 }  // namespace fa2

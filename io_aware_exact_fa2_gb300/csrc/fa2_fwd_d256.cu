@@ -27,9 +27,13 @@ namespace fa2 {
 #define FA2_D256_CS 1
 #endif
 
-fa2_status launch_fwd_d256(const LaunchArgs &a)
+using CfgD256 = FwdCfg<256, FA2_D256_BN, FA2_D256_NQ, FA2_D256_KS, FA2_D256_CS, FA2_D256_NS>;
+
+fa2_status launch_fwd_d256(const LaunchArgs &a) { return launch_fwd<CfgD256>(a); }
+
+size_t workspace_bytes_d256(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy)
 {
-    return launch_fwd<FwdCfg<256, FA2_D256_BN, FA2_D256_NQ, FA2_D256_KS, FA2_D256_CS, FA2_D256_NS>>(a);
+    return workspace_bytes_for<CfgD256>(B, H, Lq, Lk, causal, num_sms, policy);
 }
 
 }  // namespace fa2

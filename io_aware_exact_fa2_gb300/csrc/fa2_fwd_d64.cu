@@ -27,9 +27,13 @@ namespace fa2 {
 #define FA2_D64_CS 1
 #endif
 
-fa2_status launch_fwd_d64(const LaunchArgs &a)
+using CfgD64 = FwdCfg<64, FA2_D64_BN, FA2_D64_NQ, FA2_D64_KS, FA2_D64_CS, FA2_D64_NS>;
+
+fa2_status launch_fwd_d64(const LaunchArgs &a) { return launch_fwd<CfgD64>(a); }
+
+size_t workspace_bytes_d64(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy)
 {
-    return launch_fwd<FwdCfg<64, FA2_D64_BN, FA2_D64_NQ, FA2_D64_KS, FA2_D64_CS, FA2_D64_NS>>(a);
+    return workspace_bytes_for<CfgD64>(B, H, Lq, Lk, causal, num_sms, policy);
 }
 
 }  // namespace fa2

@@ -57,6 +57,14 @@ struct FwdParams {
     int n_units;                // n_qgroups * BH
     int causal;
     float scale_log2;           // scale * log2(e), > 0
+    // split schedule (non-causal, with a workspace): the n_units * n_kv K/V-tile
+    // iterations are cut into gridDim.x equal contiguous ranges, one per CTA
+    int split;                  // 0: whole units (unit_at), 1: equal tile ranges
+    int n_kv;                   // K/V tiles per unit (non-causal: ceil(Lk / BN))
+    int *counters;              // [gridDim.x][NQ] arrivals per cut unit (zero at rest)
+    float *part_lse;            // [gridDim.x][2][NQ][128][2] base-2 LSE of each part
+    float *part_o;              // [gridDim.x][2][NQ][D/4][128] float4: each part's normalised O,
+                                // column groups outermost so a warp's 32 rows are contiguous
 };
 
 // Device error codes: role in the high byte, barrier in the low byte.
@@ -94,7 +102,8 @@ struct FwdCfg {
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
     static constexpr int OFF_XMAX = OFF_V + KS * KV_TILE;           // f32 [NQ][2][CS][128]
     static constexpr int OFF_XL = OFF_XMAX + NQ * 2 * CS * 128 * 4;  // f32x2 [NQ][CS][128]
-    static constexpr int OFF_BAR = OFF_XL + NQ * CS * 128 * 8;
+    static constexpr int OFF_FLAG = OFF_XL + NQ * CS * 128 * 8;       // u32 [NQ] (+ pad)
+    static constexpr int OFF_BAR = OFF_FLAG + 16;
     static constexpr int BAR_Q_FULL = 0;                     // [NQ]
     static constexpr int BAR_Q_EMPTY = BAR_Q_FULL + NQ;      // [NQ]
     static constexpr int BAR_K_FULL = BAR_Q_EMPTY + NQ;      // [KS]
@@ -185,6 +194,63 @@ __device__ __forceinline__ void decode_unit(int idx, const FwdParams &p, int &qg
     }
 }
 
+// A stretch of work of one CTA: the K/V tiles [kv_lo, kv_hi) of a work unit.
+// Without the split schedule a segment is a whole unit (kv_hi is then taken
+// per Q tile from kv_tiles_for).  With it, a unit whose tiles straddle a CTA
+// boundary is cut: CTAs c_first..c_last each compute a part, and the last one
+// to finish combines them.
+struct Segment {
+    int unit;
+    int kv_lo, kv_hi;
+    int slot;              // this CTA's partial-result slot for the segment (0: first, 1: last)
+    int c_first, c_last;   // CTAs sharing the unit (equal for a whole unit)
+};
+
+// CTA whose tile range holds iteration x: the largest k with floor(k*I/G) <= x.
+__device__ __forceinline__ int cta_of(long long x, long long I, long long G)
+{
+    return static_cast<int>(((x + 1) * G + I - 1) / I - 1);
+}
+
+__device__ __forceinline__ long long range_begin(long long k, long long I, long long G) { return k * I / G; }
+
+__device__ __forceinline__ bool segment_at(int i, const FwdParams &p, Segment &sg)
+{
+    if (!p.split) {
+        const int u = unit_at(i, p.n_units, p.causal);
+        if (u < 0)
+            return false;
+        sg.unit = u;
+        sg.kv_lo = 0;
+        sg.kv_hi = 0x7fffffff;
+        sg.slot = 0;
+        sg.c_first = sg.c_last = static_cast<int>(blockIdx.x);
+        return true;
+    }
+    const long long I = static_cast<long long>(p.n_units) * p.n_kv;
+    const long long G = gridDim.x;
+    const long long k = blockIdx.x;
+    const long long b = range_begin(k, I, G), e = range_begin(k + 1, I, G);
+    const long long u = b / p.n_kv + i;
+    if (u * p.n_kv >= e)
+        return false;
+    sg.unit = static_cast<int>(u);
+    sg.kv_lo = static_cast<int>(b > u * p.n_kv ? b - u * p.n_kv : 0);
+    sg.kv_hi = static_cast<int>(e < (u + 1) * p.n_kv ? e - u * p.n_kv : p.n_kv);
+    sg.slot = i == 0 ? 0 : 1;
+    sg.c_first = cta_of(u * p.n_kv, I, G);
+    sg.c_last = cta_of((u + 1) * p.n_kv - 1, I, G);
+    return true;
+}
+
+// K/V tiles the Q tile starting at q0_t visits in segment sg (0 if the tile is empty).
+__device__ __forceinline__ int segment_tiles(const Segment &sg, int q0_t, const FwdParams &p, int BN)
+{
+    if (!p.split)
+        return kv_tiles_for(q0_t, p.Lq, p.Lk, p.causal, BN);
+    return q0_t < p.Lq ? sg.kv_hi - sg.kv_lo : 0;
+}
+
 // All lanes wait (bounded); the warp agrees on the outcome so warp-collective
 // tcgen05 instructions are executed by all lanes or by none.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *err, int code,
@@ -258,16 +324,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             bool k_pending = false;          // a K load of ring slot kv_iter is in flight without its V
             bool ok = true;
             for (int i = 0; ok; ++i) {
-                const int u = unit_at(i, p.n_units, p.causal);
-                if (u < 0)
+                Segment sg;
+                if (!segment_at(i, p, sg))
                     break;
                 int qg, bh;
-                decode_unit(u, p, qg, bh);
+                decode_unit(sg.unit, p, qg, bh);
                 const int q0 = qg * (C::NQ * C::BM);
                 int n_max = 0;
 #pragma unroll
                 for (int t = 0; t < C::NQ; ++t) {
-                    const int n = kv_tiles_for(q0 + t * C::BM, p.Lq, p.Lk, p.causal, C::BN);
+                    const int n = segment_tiles(sg, q0 + t * C::BM, p, C::BN);
                     n_max = max(n_max, n);
                     if (n > 0 && ok) {
                         // the buffer is free once the last S MMA of the previous unit read it
@@ -296,7 +362,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
                         tma_load_3d_hint(sbase + C::OFF_K + s * C::KV_TILE + c * C::KV_BLOCK, &tm_k, 64 * c,
-                                         j * C::BN, bh, bar(C::BAR_K_FULL + s), pol_kv);
+                                         (sg.kv_lo + j) * C::BN, bh, bar(C::BAR_K_FULL + s), pol_kv);
                     k_pending = true;
                     if (!mbar_wait(bar(C::BAR_V_EMPTY + s), ph ^ 1u, p.err, ERR_PRODUCER | 2, p.wait_limit_ns)) {
                         ok = false;
@@ -306,7 +372,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
                         tma_load_3d_hint(sbase + C::OFF_V + s * C::KV_TILE + c * C::KV_BLOCK, &tm_v, 64 * c,
-                                         j * C::BN, bh, bar(C::BAR_V_FULL + s), pol_kv);
+                                         (sg.kv_lo + j) * C::BN, bh, bar(C::BAR_V_FULL + s), pol_kv);
                     k_pending = false;
                 }
             }
@@ -343,17 +409,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         bool ok = true;
 
         for (int i = 0; ok; ++i) {
-            const int u = unit_at(i, p.n_units, p.causal);
-            if (u < 0)
+            Segment sg;
+            if (!segment_at(i, p, sg))
                 break;
             int qg, bh;
-            decode_unit(u, p, qg, bh);
+            decode_unit(sg.unit, p, qg, bh);
             const int q0 = qg * (C::NQ * C::BM);
             int n_t[C::NQ];
             int n_max = 0;
 #pragma unroll
             for (int t = 0; t < C::NQ; ++t) {
-                n_t[t] = kv_tiles_for(q0 + t * C::BM, p.Lq, p.Lk, p.causal, C::BN);
+                n_t[t] = segment_tiles(sg, q0 + t * C::BM, p, C::BN);
                 n_max = max(n_max, n_t[t]);
             }
             // the last Q tile (highest t) that reads K/V tile j
@@ -481,21 +547,22 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const uint32_t xmax = sbase + C::OFF_XMAX + t * (2 * C::CS * 128 * 4);
         const uint32_t xl = sbase + C::OFF_XL + t * (C::CS * 128 * 8);
         const float c2 = p.scale_log2;
-        uint32_t tbase = 0;    // S tiles of this slot in earlier units (running phase base)
-        uint32_t units = 0;    // earlier units of this slot
+        uint32_t tbase = 0;    // S tiles of this slot in earlier segments (running phase base)
+        uint32_t group_uses = 0;   // completed phases of this slot's group barrier
         bool ok = true;
 
         for (int i = 0; ok; ++i) {
-            const int u = unit_at(i, p.n_units, p.causal);
-            if (u < 0)
+            Segment sg;
+            if (!segment_at(i, p, sg))
                 break;
             int qg, bh;
-            decode_unit(u, p, qg, bh);
+            decode_unit(sg.unit, p, qg, bh);
             const int q0_t = qg * (C::NQ * C::BM) + t * C::BM;
             const int grow = q0_t + row;             // query index
-            const int n = kv_tiles_for(q0_t, p.Lq, p.Lk, p.causal, C::BN);
+            const int n = segment_tiles(sg, q0_t, p, C::BN);
             if (n == 0)
                 continue;
+            const int kv0 = p.split ? sg.kv_lo : 0;  // absolute index of the segment's first K/V tile
             float m_use = -INFINITY;   // running max (log2 domain, possibly stale by < 2^THRESHOLD)
             float l = 0.f;             // running normaliser of the fp32 weights (for LSE)
             float l_o = 0.f;           // running normaliser of the bf16 weights the PV MMA sees (for O)
@@ -527,8 +594,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 }
 
                 // mask: key tail (j >= Lk) and, on tiles crossing the diagonal, causal j > i
-                const int k0 = j * C::BN + h * C::NCOL;
-                if ((p.causal && j * C::BN + C::BN - 1 > q0_t) || (j * C::BN + C::BN > p.Lk)) {
+                const int jj = kv0 + j;                  // absolute K/V tile
+                const int k0 = jj * C::BN + h * C::NCOL;
+                if ((p.causal && jj * C::BN + C::BN - 1 > q0_t) || (jj * C::BN + C::BN > p.Lk)) {
                     const int lim = p.causal ? min(grow + 1, p.Lk) : p.Lk;  // keys < lim are visible
 #pragma unroll
                     for (int c = 0; c < C::NCOL; ++c)
@@ -564,9 +632,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 }
                 const float m_tile = mx * c2;
 
-                // The first tile always holds key 0, which every row may see, so m_tile is
-                // finite there; later tiles keep the stale max unless it grows a lot.  All
-                // slices of a row see the same m_tile and so take the same decision.
+                // The first tile of a segment always holds a key every row may see (key 0
+                // for whole units; any tile for the non-causal split schedule), so m_tile
+                // is finite there; later tiles keep the stale max unless it grows a lot.
+                // All slices of a row see the same m_tile and so take the same decision.
                 float alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
@@ -664,18 +733,25 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 break;
 
             // ---- epilogue: O out of TMEM (then released to the MMA warp), O / l -> bf16
-            // rows and LSE straight to global memory
+            // rows and LSE straight to global memory; a cut unit's part goes to the
+            // workspace first and the last part to finish combines all of them
             const uint32_t g_last = tbase + n - 1;
             ok = warp_wait(bar(C::BAR_O_DONE + t), g_last & 1, p.err, ERR_SOFTMAX | 3, p.wait_limit_ns);
             if (!ok)
                 break;
+            // all threads of this slot's group arrive, then wait for the phase to complete
+            auto group_sync = [&](int code) -> bool {
+                mbar_arrive(bar(C::BAR_GROUP + t));
+                const bool r = warp_wait(bar(C::BAR_GROUP + t), group_uses & 1, p.err, ERR_SOFTMAX | code,
+                                         p.wait_limit_ns);
+                ++group_uses;
+                return r;
+            };
             float l_tot = l, lo_tot = l_o;
             if constexpr (C::CS > 1) {
                 st_shared_f32(xl + (h * 128 + row) * 8, l);
                 st_shared_f32(xl + (h * 128 + row) * 8 + 4, l_o);
-                mbar_arrive(bar(C::BAR_GROUP + t));
-                ok = warp_wait(bar(C::BAR_GROUP + t), units & 1, p.err, ERR_SOFTMAX | 5, p.wait_limit_ns);
-                if (!ok)
+                if (!(ok = group_sync(5)))
                     break;
                 l_tot = 0.f;
                 lo_tot = 0.f;
@@ -687,34 +763,206 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             tc_fence_after();
             const float inv_l = 1.f / lo_tot;
-            const float lse = (m_use + lg2_approx(l_tot)) * LN2;
             const bool live = grow < p.Lq;
-            uint16_t *orow = p.o + (static_cast<size_t>(bh) * p.Lq + (live ? grow : 0)) * C::D + h * C::OCOL;
-#pragma unroll 1
-            for (int cc = 0; cc < C::OCOL / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32(o_addr + 32 * cc, r);
-                tmem_ld_wait(r);
-                if (cc == C::OCOL / 32 - 1) {
-                    // every read of O_t is done: the next unit's first PV may overwrite it
-                    tc_fence_before();
-                    mbar_arrive(bar(C::BAR_O_FREE + t));
+            const size_t out_row = static_cast<size_t>(bh) * p.Lq + (live ? grow : 0);
+            uint16_t *orow = p.o + out_row * C::D + h * C::OCOL;
+            const bool whole = sg.c_first == sg.c_last;
+            // this part's workspace rows (cut units only): LSE pairs by row, O as float4
+            // column groups of 128 rows each
+            const size_t part_tile = (static_cast<size_t>(blockIdx.x) * 2 + sg.slot) * C::NQ + t;
+            const size_t part_row = part_tile * 128 + row;
+            const int n_parts = sg.c_last - sg.c_first + 1;
+            int *counter = p.counters + sg.c_first * C::NQ + t;
+            const uint32_t flag = sbase + C::OFF_FLAG + 4 * t;
+            // Part statistics (base 2): lse_o weighs this part's O (its bf16 mass, the
+            // normaliser O was divided by), lse_x is its exact log-sum-exp.
+            const float own_lse_o = m_use + lg2_approx(lo_tot);
+            const float own_lse_x = m_use + lg2_approx(l_tot);
+
+            // Merge of all parts of a cut unit into bf16 O and LSE.  Each part's O is
+            // taken as its fp32 values divided by its own normaliser, and the parts are
+            // summed in CTA order two at a time, so the result does not depend on which
+            // CTA merges or on whether its own part comes from TMEM or the workspace.
+            auto combine = [&](bool own_from_tmem) {
+                const long long I = static_cast<long long>(p.n_units) * p.n_kv;
+                const long long G = gridDim.x;
+                // The slot of part c: every CTA after the unit's first one starts its
+                // range inside the unit, so the unit is its first segment (slot 0); the
+                // first CTA used slot 0 only if its range starts exactly at the unit's
+                // first tile.
+                const int first_slot =
+                    range_begin(sg.c_first, I, G) == static_cast<long long>(sg.unit) * p.n_kv ? 0 : 1;
+                auto tile_of = [&](int c) -> size_t {
+                    return (static_cast<size_t>(c) * 2 + (c == sg.c_first ? first_slot : 0)) * C::NQ + t;
+                };
+                const int self = own_from_tmem ? static_cast<int>(blockIdx.x) : -1;
+                auto lse_o_of = [&](int c) {
+                    return c == self ? own_lse_o : __ldcg(p.part_lse + (tile_of(c) * 128 + row) * 2);
+                };
+                // combine weights: O parts by their bf16 masses (lse_o), LSE exactly
+                float mo = -INFINITY, mx = -INFINITY;
+                for (int c = sg.c_first; c <= sg.c_last; ++c) {
+                    mo = fmaxf(mo, lse_o_of(c));
+                    mx = fmaxf(mx, c == self ? own_lse_x : __ldcg(p.part_lse + (tile_of(c) * 128 + row) * 2 + 1));
                 }
-                uint32_t w[16];
+                float wsum = 0.f, xsum = 0.f;
+                for (int c = sg.c_first; c <= sg.c_last; ++c) {
+                    wsum += ex2_approx(lse_o_of(c) - mo);
+                    xsum += ex2_approx((c == self ? own_lse_x : __ldcg(p.part_lse + (tile_of(c) * 128 + row) * 2 + 1)) - mx);
+                }
+                const float inv_w = 1.f / wsum;
+                const float4 *part4 = reinterpret_cast<const float4 *>(p.part_o);
+#pragma unroll 1
+                for (int cc = 0; cc < C::OCOL / 32; ++cc) {
+                    const size_t col4 = static_cast<size_t>((h * C::OCOL + 32 * cc) / 4) * 128 + row;
+                    // this CTA's own part, read out of TMEM when its turn in the sum comes
+                    auto load_own = [&](float4 *dst) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + 32 * cc, r);
+                        tmem_ld_wait(r);
+                        if (cc == C::OCOL / 32 - 1) {
+                            tc_fence_before();
+                            mbar_arrive(bar(C::BAR_O_FREE + t));
+                        }
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-                if (live) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(r[4 * q]) * inv_l, __uint_as_float(r[4 * q + 1]) * inv_l,
+                                                 __uint_as_float(r[4 * q + 2]) * inv_l,
+                                                 __uint_as_float(r[4 * q + 3]) * inv_l);
+                    };
+                    float acc[32];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    for (int e = 0; e < 32; ++e)
+                        acc[e] = 0.f;
+                    // two parts per step, so 16 loads are in flight per round trip
+                    for (int c = sg.c_first; c <= sg.c_last; c += 2) {
+                        const bool two = c + 1 <= sg.c_last;
+                        const size_t ta = tile_of(c), tb = two ? tile_of(c + 1) : ta;
+                        const float wa = ex2_approx(lse_o_of(c) - mo) * inv_w;
+                        const float wb = two ? ex2_approx(lse_o_of(c + 1) - mo) * inv_w : 0.f;
+                        const float4 *sa = part4 + ta * (C::D / 4) * 128 + col4;
+                        const float4 *sb = part4 + tb * (C::D / 4) * 128 + col4;
+                        const bool a_own = c == self, b_own = two && c + 1 == self;
+                        float4 va[8], vb[8];
+                        if (a_own) {
+                            load_own(va);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                va[q] = __ldcg(sa + q * 128);
+                        }
+                        if (b_own) {
+                            load_own(vb);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                vb[q] = __ldcg(sb + q * 128);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            acc[4 * q] += wa * va[q].x + wb * vb[q].x;
+                            acc[4 * q + 1] += wa * va[q].y + wb * vb[q].y;
+                            acc[4 * q + 2] += wa * va[q].z + wb * vb[q].z;
+                            acc[4 * q + 3] += wa * va[q].w + wb * vb[q].w;
+                        }
+                    }
+                    if (live) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(pack_bf16x2(acc[8 * q], acc[8 * q + 1]),
+                                                pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]),
+                                                pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]),
+                                                pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]));
+                    }
+                }
+                if (h == 0 && live)
+                    p.lse[out_row] = (mx + lg2_approx(xsum)) * LN2;
+            };
+
+            // A cut unit's part that finds every other part already published merges
+            // straight from TMEM; otherwise it publishes itself first.
+            bool direct = false;
+            if (!whole) {
+                if (h == 0 && row == 0) {
+                    const int arrived = ld_acquire_gpu(counter);
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(flag), "r"(arrived == n_parts - 1 ? 1 : 0)
+                                 : "memory");
+                }
+                if (!(ok = group_sync(6)))
+                    break;
+                uint32_t d;
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(d) : "r"(flag) : "memory");
+                direct = d != 0;
+            }
+            if (direct) {
+                fence_acq_rel_gpu();
+                combine(true);
+                if (h == 0 && row == 0)
+                    atomicExch(counter, 0);   // leave the workspace ready for the next call
+            } else {
+                float4 *ptile = whole ? nullptr : reinterpret_cast<float4 *>(p.part_o) + part_tile * (C::D / 4) * 128;
+#pragma unroll 1
+                for (int cc = 0; cc < C::OCOL / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32(o_addr + 32 * cc, r);
+                    tmem_ld_wait(r);
+                    if (cc == C::OCOL / 32 - 1) {
+                        // every read of O_t is done: the next segment's first PV may overwrite it
+                        tc_fence_before();
+                        mbar_arrive(bar(C::BAR_O_FREE + t));
+                    }
+                    if (whole) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
+                                               __uint_as_float(r[2 * e + 1]) * inv_l);
+                        if (live) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                        }
+                    } else {
+                        const int g0 = (h * C::OCOL + 32 * cc) / 4;   // first float4 column group
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            ptile[(g0 + q) * 128 + row] = make_float4(
+                                __uint_as_float(r[4 * q]) * inv_l, __uint_as_float(r[4 * q + 1]) * inv_l,
+                                __uint_as_float(r[4 * q + 2]) * inv_l, __uint_as_float(r[4 * q + 3]) * inv_l);
+                    }
+                }
+                if (whole) {
+                    if (h == 0 && live)
+                        p.lse[out_row] = (m_use + lg2_approx(l_tot)) * LN2;
+                } else {
+                    if (h == 0) {
+                        p.part_lse[part_row * 2] = own_lse_o;
+                        p.part_lse[part_row * 2 + 1] = own_lse_x;
+                    }
+                    // publish the part, count it, and let the last part in do the merge
+                    fence_acq_rel_gpu();
+                    if (!(ok = group_sync(7)))
+                        break;
+                    if (h == 0 && row == 0) {
+                        const int before = atomicAdd(counter, 1);
+                        const int last = before == n_parts - 1;
+                        if (last)
+                            atomicExch(counter, 0);   // leave the workspace ready for the next call
+                        asm volatile("st.shared.u32 [%0], %1;" ::"r"(flag), "r"(last) : "memory");
+                    }
+                    if (!(ok = group_sync(8)))
+                        break;
+                    uint32_t last;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(last) : "r"(flag) : "memory");
+                    if (last) {
+                        fence_acq_rel_gpu();
+                        combine(false);
+                    }
                 }
             }
-            if (h == 0 && live)
-                p.lse[static_cast<size_t>(bh) * p.Lq + grow] = lse;
             tbase += n;
-            ++units;
         }
     }
 

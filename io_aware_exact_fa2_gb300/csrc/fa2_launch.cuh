@@ -29,7 +29,70 @@ struct LaunchArgs {
     EncodeTiledFn encode;
     int device;
     int num_sms;    // streaming multiprocessors of `device`
+    int split_policy;         // SPLIT_NEVER / SPLIT_AUTO / SPLIT_ALWAYS
+    void *workspace;          // optional (split schedule for non-causal passes)
+    size_t workspace_bytes;
 };
+
+// Workspace of the split schedule for a launch of G CTAs: arrival counters,
+// then per CTA two part slots of NQ x 128 rows: an LSE pair per row, and O in
+// fp32 (stored by 4-column groups of 128 rows).
+struct WorkspaceLayout {
+    size_t counters, part_lse, part_o, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+inline WorkspaceLayout workspace_layout(long long G, int NQ, int D)
+{
+    WorkspaceLayout w;
+    w.counters = 0;
+    w.part_lse = align256(static_cast<size_t>(G) * NQ * sizeof(int));
+    w.part_o = w.part_lse + align256(static_cast<size_t>(G) * 2 * NQ * 128 * 2 * sizeof(float));
+    w.total = w.part_o + align256(static_cast<size_t>(G) * 2 * NQ * 128 * D * sizeof(float));
+    return w;
+}
+
+// Grid of the split schedule: one CTA per SM, at most one per K/V-tile iteration.
+inline long long split_grid(long long n_units, long long n_kv, int num_sms)
+{
+    const long long iters = n_units * n_kv;
+    return iters < num_sms ? iters : num_sms;
+}
+
+// Whether cutting the K/V-tile iterations into equal per-SM ranges beats
+// dealing out whole units, in K/V-tile times: whole units finish after
+// ceil(units / SMs) units of n_kv tiles; equal ranges after ceil(units * n_kv
+// / SMs) tiles plus the cost of writing and merging the cut parts (measured on
+// GB300 at about six tile times).  Only taken when it saves at least 5 %.
+inline bool split_pays(long long units, long long n_kv, int num_sms)
+{
+    constexpr long long kPartOverheadTiles = 6;
+    const long long whole = (units + num_sms - 1) / num_sms * n_kv;
+    const long long split = (units * n_kv + num_sms - 1) / num_sms + kPartOverheadTiles;
+    return split * 100 < whole * 95;
+}
+
+enum SplitPolicy { SPLIT_NEVER = 0, SPLIT_AUTO = 1, SPLIT_ALWAYS = 2 };
+
+inline bool use_split(int policy, long long units, long long n_kv, int num_sms)
+{
+    return policy == SPLIT_ALWAYS || (policy == SPLIT_AUTO && split_pays(units, n_kv, num_sms));
+}
+
+// Bytes of workspace the pass needs for its split schedule (0: none is used).
+template <class C>
+size_t workspace_bytes_for(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy)
+{
+    if (causal || Lq <= 0)
+        return 0;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long units = ((Lq + C::NQ * C::BM - 1) / (C::NQ * C::BM)) * BH;
+    const long long n_kv = (Lk + C::BN - 1) / C::BN;
+    if (!use_split(policy, units, n_kv, num_sms))
+        return 0;
+    return workspace_layout(split_grid(units, n_kv, num_sms), C::NQ, C::D).total;
+}
 
 // 3-D view of a contiguous bf16 [B*H, L, D] tensor: dims (D, L, B*H) innermost
 // first, a box of 64 columns (128 bytes, one swizzle span) by box_rows rows by
@@ -74,8 +137,24 @@ fa2_status launch_fwd(const LaunchArgs &a)
     if (units > INT_MAX)
         return FA2_ERR_INVALID_ARG;
     p.n_units = static_cast<int>(units);
-    // persistent grid: one CTA per SM (each holds all of TMEM), walking the units
-    const long long grid = units < a.num_sms ? units : a.num_sms;
+    p.n_kv = (a.Lk + C::BN - 1) / C::BN;
+    // persistent grid: one CTA per SM (each holds all of TMEM), walking the units;
+    // non-causal passes with a workspace cut the tile iterations into equal ranges
+    p.split = (!a.causal && a.workspace != nullptr && use_split(a.split_policy, units, p.n_kv, a.num_sms)) ? 1 : 0;
+    long long grid = units < a.num_sms ? units : a.num_sms;
+    p.counters = nullptr;
+    p.part_lse = nullptr;
+    p.part_o = nullptr;
+    if (p.split) {
+        grid = split_grid(units, p.n_kv, a.num_sms);
+        const WorkspaceLayout w = workspace_layout(grid, C::NQ, C::D);
+        if (a.workspace_bytes < w.total)
+            return FA2_ERR_INVALID_ARG;
+        char *base = static_cast<char *>(a.workspace);
+        p.counters = reinterpret_cast<int *>(base + w.counters);
+        p.part_lse = reinterpret_cast<float *>(base + w.part_lse);
+        p.part_o = reinterpret_cast<float *>(base + w.part_o);
+    }
 
     // opt in to more than 48 KB of dynamic shared memory, once per device
     static std::atomic<unsigned long long> configured{0};
@@ -96,5 +175,8 @@ fa2_status launch_fwd(const LaunchArgs &a)
 fa2_status launch_fwd_d64(const LaunchArgs &a);
 fa2_status launch_fwd_d128(const LaunchArgs &a);
 fa2_status launch_fwd_d256(const LaunchArgs &a);
+size_t workspace_bytes_d64(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy);
+size_t workspace_bytes_d128(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy);
+size_t workspace_bytes_d256(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy);
 
 }  // namespace fa2

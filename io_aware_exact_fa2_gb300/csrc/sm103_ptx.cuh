@@ -167,6 +167,17 @@ __device__ __forceinline__ void tma_store_wait_read_all()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Release this thread's prior writes / acquire others' at GPU scope (cumulative
+// over what this thread has observed, e.g. through a CTA barrier).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *ptr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_proxy_async_smem()
 {

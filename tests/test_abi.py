@@ -32,8 +32,8 @@ def header_functions():
 
 
 def test_header_declares_the_boundary():
-    assert header_functions() == ["fa2_fwd", "fa2_fwd_from_host", "fa2_get_device_error",
-                                  "fa2_status_string", "fa2_version"]
+    assert header_functions() == ["fa2_fwd", "fa2_fwd_from_host", "fa2_fwd_ws", "fa2_get_device_error",
+                                  "fa2_status_string", "fa2_version", "fa2_workspace_size"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -96,6 +96,25 @@ def test_from_host_validation(lib):
     assert f(*bad, 1, 1, 8, 8, 64, 0, 0.125, None) == INVALID
     assert f(*args, 1, 1, 8, 8, 80, 0, 0.125, None) == UNSUPPORTED
     assert f(*args, 1, 1, 0, 8, 64, 0, 0.125, None) == OK
+
+
+def test_workspace_entry_points_validation(lib):
+    n = ctypes.c_size_t(123)
+    f = lib.fa2_workspace_size
+    assert f(1, 1, 8, 8, 64, 0, 0, None) == INVALID
+    assert f(0, 1, 8, 8, 64, 0, 0, ctypes.byref(n)) == INVALID and n.value == 0
+    assert f(1, 1, 8, 8, 96, 0, 0, ctypes.byref(n)) == UNSUPPORTED
+    assert f(1, 1, 8, 8, 64, 1, 0, ctypes.byref(n)) == OK and n.value == 0   # causal: none needed
+    assert f(1, 1, 0, 8, 64, 0, 0, ctypes.byref(n)) == OK and n.value == 0   # Lq == 0
+    g = lib.fa2_fwd_ws
+    args = [P] * 5 + [1, 1, 8, 8, 64, 0, 0.125]
+    assert g(*args, P + 16, 1 << 20, None) == INVALID     # workspace not 256-byte aligned
+    bad = list(args)
+    bad[9] = 80
+    assert g(*bad, P, 1 << 20, None) == UNSUPPORTED
+    zero_q = list(args)
+    zero_q[7] = 0
+    assert g(*zero_q, 0, 0, None) == OK                   # Lq == 0 is a no-op
 
 
 def test_no_gpu_reports_cuda_error_instead_of_crashing(lib):

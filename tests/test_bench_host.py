@@ -41,7 +41,7 @@ def test_clock_summary():
 
 def test_traffic_record_tracks_kernel_source(tmp_path, monkeypatch):
     from io_aware_exact_fa2_gb300 import build as fa2_build
-    digest = fa2_build.source_digest()
+    digest = fa2_build.kernel_digest()
     rec = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if os.path.exists(rec):
         d = json.load(open(rec))

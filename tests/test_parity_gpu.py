@@ -74,6 +74,71 @@ def test_many_units_per_cta(D, causal):
     check(8, 20, 300, 457, D, causal, seed=650 + D)
 
 
+def run_ws(q, k, v, causal, scale, ws=None):
+    """fa2_fwd_ws on seeded CPU inputs (workspace from fa2_workspace unless given)."""
+    from io_aware_exact_fa2_gb300 import fa2_fwd, fa2_get_device_error, fa2_workspace
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    B, H, Lq, D = q.shape
+    if ws is None:
+        ws = fa2_workspace(qd, kd, causal)
+    o = torch.full((B, H, Lq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((B, H, Lq), float("nan"), dtype=torch.float32, device=dev)
+    fa2_fwd(qd, kd, vd, o, lse, causal, scale, workspace=ws)
+    st, code = fa2_get_device_error()
+    assert st == 0, f"device error {code:#x}"
+    return o.cpu(), lse.cpu(), ws
+
+
+@pytest.fixture
+def split_always(monkeypatch):
+    """Force the cut-range schedule whenever a workspace is given (small shapes
+    would otherwise be estimated not to gain from it)."""
+    monkeypatch.setenv("FA2_SPLIT", "always")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("shape", [(8, 20, 300, 457), (2, 3, 640, 1000), (1, 4, 129, 1), (3, 5, 130, 190),
+                                   (1, 1, 1000, 4096)])
+def test_split_schedule_matches_oracle(D, shape, split_always):
+    """Non-causal with a workspace: key-tile ranges cut across SMs, cut query tiles
+    computed in parts and merged; every element against the oracle."""
+    B, H, Lq, Lk = shape
+    q, k, v = make_qkv(B, H, Lq, Lk, D, seed_base=1500 + D + Lq)
+    o, lse, ws = run_ws(q, k, v, False, scale_of(D))
+    o_ref, lse_ref = oracle.attention(q, k, v, False, scale_of(D))
+    compare(o, lse, o_ref, lse_ref)
+    # the arrival counters at the start of the workspace are zero again
+    assert torch.count_nonzero(ws[:256]) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_split_schedule_deterministic_and_reusable(D, split_always):
+    """Same inputs and workspace twice -> bit-identical output; causal ignores the workspace."""
+    q, k, v = make_qkv(4, 8, 500, 700, D, seed_base=1600 + D)
+    a = run_ws(q, k, v, False, scale_of(D))
+    b = run_ws(q, k, v, False, scale_of(D), ws=a[2])
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    c_ws = run_ws(q, k, v, True, scale_of(D), ws=a[2])
+    c_plain = run_cuda(q, k, v, True, scale_of(D))
+    assert torch.equal(c_ws[0], c_plain[0]) and torch.equal(c_ws[1], c_plain[1])
+
+
+def test_split_cost_model(monkeypatch):
+    """The default estimate takes the cut ranges for one long head (4 query tiles on
+    152+ SMs) and not for many short heads; FA2_SPLIT=never/always override it."""
+    from io_aware_exact_fa2_gb300 import fa2_workspace_size
+    monkeypatch.delenv("FA2_SPLIT", raising=False)
+    assert fa2_workspace_size(1, 1, 1000, 4096, 128, False) > 0
+    assert fa2_workspace_size(8, 20, 300, 457, 128, False) == 0
+    assert fa2_workspace_size(1, 1, 1000, 4096, 128, True) == 0
+    monkeypatch.setenv("FA2_SPLIT", "never")
+    assert fa2_workspace_size(1, 1, 1000, 4096, 128, False) == 0
+    monkeypatch.setenv("FA2_SPLIT", "always")
+    assert fa2_workspace_size(8, 20, 300, 457, 128, False) > 0
+    assert fa2_workspace_size(8, 20, 300, 457, 128, True) == 0
+
+
 def test_lq_zero_is_a_noop():
     """Lq == 0: FA2_OK and nothing is written."""
     from io_aware_exact_fa2_gb300 import _binding
