@@ -27,11 +27,14 @@
  *   - D must be 64, 128 or 256.  scale must be finite and > 0 (the pages use
  *     1/sqrt(D)).  Causal with Lq != Lk uses the top-left rule j <= i.
  *   - Device pointers must be 16-byte aligned (TMA requirement); lse 4-byte.
- *   - The caller owns every buffer.  No entry point allocates device memory.
+ *   - The caller owns every buffer, except the fixed scratch that
+ *     fa2_fwd_noalloc takes from the library.  No entry point allocates
+ *     device memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are stream-ordered and asynchronous: they return once
  *     the work is enqueued, and never synchronise except where stated.
- *   - Re-entrant and thread-safe; the library keeps no per-call state.
+ *   - Re-entrant and thread-safe; the library keeps no per-call state (but
+ *     calls of fa2_fwd_noalloc that overlap on the GPU share its scratch).
  *   - O and LSE rows i >= Lq are never written; inputs are never written.
  */
 #ifndef FA2_GB300_H
@@ -122,6 +125,44 @@ fa2_status fa2_fwd_ws(const void *q, const void *k, const void *v, void *o,
                       float *lse, int B, int H, int Lq, int Lk, int D,
                       int causal, float scale, void *workspace,
                       size_t workspace_bytes, void *stream);
+
+/*
+ * fa2_fwd_noalloc -- fa2_fwd_ws for callers that may not allocate device
+ * memory, with the workspace taken from a fixed scratch buffer that lives in
+ * the library itself (FA2_NOALLOC_SCRATCH_BYTES per device).  The FlashAttention
+ * write-ups this library follows have no counterpart to this entry point.
+ *
+ * Who cannot allocate: code hosted inside a framework that owns every byte of
+ * device memory through its own pool and budget (a plug-in may only use the
+ * pointers it is handed, since a side cudaMalloc would escape that budget),
+ * and latency-critical loops that rule out cudaMalloc / cudaFree because
+ * either can synchronise the device and take unbounded time.  This entry point
+ * calls neither, nor any routine that allocates.
+ *
+ * Same arguments, outputs, schedule and results (bit for bit) as fa2_fwd_ws
+ * given a workspace of fa2_workspace_size() bytes.
+ *
+ *   - The first call on a device does the set-up: it looks up the scratch's
+ *     device address with that device current (and the CUDA module holding it
+ *     is loaded then).  Make that first call before any stream capture.
+ *   - Each call clears the arrival counters at the start of the scratch (the
+ *     only part that must start at zero) with a memset enqueued on `stream`,
+ *     ahead of the kernel.
+ *   - The scratch is one buffer per device, shared by every call: calls that
+ *     overlap on the GPU (e.g. enqueued on different streams without ordering
+ *     between them) race on it and their outputs are undefined.  Order them
+ *     on one stream, or use fa2_fwd_ws with a workspace per stream.
+ *
+ * Errors: as fa2_fwd_ws; FA2_ERR_UNSUPPORTED when the pass needs more than
+ * FA2_NOALLOC_SCRATCH_BYTES of workspace (fa2_workspace_size() tells how much
+ * it needs; no shape does on a GPU with at most 152 SMs); FA2_ERR_CUDA if the
+ * scratch cannot be looked up or cleared.
+ */
+#define FA2_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
+
+fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
+                           float *lse, int B, int H, int Lq, int Lk, int D,
+                           int causal, float scale, void *stream);
 
 /*
  * fa2_fwd_from_host -- the same pass starting from, and ending in, HOST

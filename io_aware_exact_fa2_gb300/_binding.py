@@ -12,6 +12,9 @@ import os
 
 from .build import LIB_PATH
 
+# FA2_NOALLOC_SCRATCH_BYTES of include/fa2.h: the fixed workspace of fa2_fwd_noalloc
+NOALLOC_SCRATCH_BYTES = 48 << 20
+
 STATUS = {0: "FA2_OK", 1: "FA2_ERR_INVALID_ARG", 2: "FA2_ERR_UNSUPPORTED",
           3: "FA2_ERR_CUDA", 4: "FA2_ERR_TIMEOUT"}
 
@@ -41,6 +44,8 @@ def load_library() -> ctypes.CDLL:
     lib.fa2_workspace_size.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.fa2_fwd_ws.restype = i
     lib.fa2_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.fa2_fwd_noalloc.restype = i
+    lib.fa2_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa2_get_device_error.restype = i
     lib.fa2_get_device_error.argtypes = [vp, ctypes.POINTER(i)]
     lib.fa2_status_string.restype = ctypes.c_char_p
@@ -122,6 +127,30 @@ def fa2_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=No
         where = "fa2_fwd_ws"
     if st != 0:
         raise Fa2Error(st, where)
+
+
+def fa2_fwd_noalloc(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:
+    """fa2_fwd with a workspace for callers that may not allocate device memory.
+
+    Runs the same schedule as fa2_fwd(..., workspace=fa2_workspace(q, k, causal)),
+    with the workspace taken from the library's fixed per-device scratch
+    (NOALLOC_SCRATCH_BYTES) instead: neither this function nor the library
+    allocates.  Calls that overlap on the GPU share that scratch and race.
+    """
+    B, H, Lq, Lk, D = _check_shapes(q, k, v, o, lse)
+    for t in (q, k, v, o, lse):
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+    if scale is None:
+        scale = D ** -0.5
+    st = _lib.fa2_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              B, H, Lq, Lk, D, int(bool(causal)), float(scale), _stream_handle(stream, q.device))
+    if st == 2 and D in (64, 128, 256):
+        need = fa2_workspace_size(B, H, Lq, Lk, D, causal, q.device.index or 0)
+        raise Fa2Error(st, f"fa2_fwd_noalloc (needs {need} bytes of workspace, "
+                           f"the fixed scratch holds {NOALLOC_SCRATCH_BYTES})")
+    if st != 0:
+        raise Fa2Error(st, "fa2_fwd_noalloc")
 
 
 def fa2_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,

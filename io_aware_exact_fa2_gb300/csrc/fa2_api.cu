@@ -21,6 +21,9 @@ namespace fa2 {
 // Written by a kernel when one of its bounded waits runs out (first code wins).
 static __device__ int g_device_error;
 
+// Device address of fa2_fwd_noalloc's fixed scratch on `dev` (fa2_noalloc.cu).
+void *noalloc_scratch_ptr(int dev);
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -230,6 +233,38 @@ FA2_EXPORT fa2_status fa2_fwd_ws(const void *q, const void *k, const void *v, vo
         return FA2_ERR_INVALID_ARG;
     return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, static_cast<cudaStream_t>(stream),
                        workspace, workspace_bytes);
+}
+
+FA2_EXPORT fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                                      int H, int Lq, int Lk, int D, int causal, float scale, void *stream)
+{
+    fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
+    if (st != FA2_OK || Lq == 0)
+        return st;
+    int dev = 0;
+    if ((st = fa2::select_device_of(q, &dev)) != FA2_OK)
+        return st;
+    const int sms = fa2::sm_count(dev);
+    if (sms <= 0)
+        return FA2_ERR_CUDA;
+    const size_t need = fa2::workspace_bytes(B, H, Lq, Lk, D, causal, sms);
+    if (need > FA2_NOALLOC_SCRATCH_BYTES)
+        return FA2_ERR_UNSUPPORTED;   // more workspace than the fixed scratch holds
+    void *scratch = nullptr;
+    if (need > 0) {
+        scratch = fa2::noalloc_scratch_ptr(dev);
+        if (!scratch)
+            return FA2_ERR_CUDA;
+        // the arrival counters (one int per CTA and Q tile, at most 2 Q tiles) start at zero
+        const size_t zero_bytes = fa2::align256(static_cast<size_t>(sms) * 2 * sizeof(int));
+        if (cudaMemsetAsync(scratch, 0, zero_bytes < need ? zero_bytes : need, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return FA2_ERR_CUDA;
+        }
+    }
+    return fa2_fwd_ws(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, scratch, FA2_NOALLOC_SCRATCH_BYTES,
+                      stream);
 }
 
 FA2_EXPORT fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,

@@ -32,8 +32,9 @@ def header_functions():
 
 
 def test_header_declares_the_boundary():
-    assert header_functions() == ["fa2_fwd", "fa2_fwd_from_host", "fa2_fwd_ws", "fa2_get_device_error",
-                                  "fa2_status_string", "fa2_version", "fa2_workspace_size"]
+    assert header_functions() == ["fa2_fwd", "fa2_fwd_from_host", "fa2_fwd_noalloc", "fa2_fwd_ws",
+                                  "fa2_get_device_error", "fa2_status_string", "fa2_version",
+                                  "fa2_workspace_size"]
 
 
 def test_library_exports_every_declared_symbol(lib):
