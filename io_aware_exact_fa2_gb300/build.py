@@ -41,7 +41,7 @@ def nvcc() -> str:
 def source_digest() -> str:
     """Hash of every kernel/host source and the public header (for staleness checks)."""
     h = hashlib.sha256()
-    files = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
+    files = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h")))
     for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
@@ -57,7 +57,7 @@ def kernel_digest() -> str:
     across host-only changes."""
     h = hashlib.sha256()
     files = sorted(f for f in os.listdir(CSRC)
-                   if f in ("fa2_fwd_kernel.cuh", "sm103_ptx.cuh", "fa2_launch.cuh")
+                   if f in ("fa2_fwd_kernel.cuh", "sm103_ptx.cuh", "fa2_launch.cuh", "fa2_split_ranges.h")
                    or (f.startswith("fa2_fwd_d") and f.endswith(".cu")))
     for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:

@@ -42,6 +42,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "fa2_split_ranges.h"
 #include "sm103_ptx.cuh"
 
 namespace fa2 {
@@ -58,13 +59,21 @@ struct FwdParams {
     int causal;
     float scale_log2;           // scale * log2(e), > 0
     // split schedule (non-causal, with a workspace): the n_units * n_kv K/V-tile
-    // iterations are cut into gridDim.x equal contiguous ranges, one per CTA
-    int split;                  // 0: whole units (unit_at), 1: equal tile ranges
+    // iterations are cut into gridDim.x contiguous ranges, one per CTA, of equal cost
+    // (tiles plus a fixed cost per unit or part of a unit the range touches)
+    int split;                  // 0: whole units (unit_at), 1: cost-balanced tile ranges
     int n_kv;                   // K/V tiles per unit (non-causal: ceil(Lk / BN))
     int *counters;              // [gridDim.x][NQ] arrivals per cut unit (zero at rest)
     float *part_lse;            // [gridDim.x][2][NQ][128][2] base-2 LSE of each part
     float *part_o;              // [gridDim.x][2][NQ][D/4][128] float4: each part's normalised O,
                                 // column groups outermost so a warp's 32 rows are contiguous
+};
+
+// Ranges of the split schedule: CTA k works on iterations [begin[k], begin[k + 1]).
+// A kernel parameter of its own (grid-constant, indexed in place), so the other
+// parameters keep their register-resident layout.
+struct SplitRanges {
+    int begin[MAX_SPLIT_CTAS + 1];
 };
 
 // Device error codes: role in the high byte, barrier in the low byte.
@@ -206,15 +215,21 @@ struct Segment {
     int c_first, c_last;   // CTAs sharing the unit (equal for a whole unit)
 };
 
-// CTA whose tile range holds iteration x: the largest k with floor(k*I/G) <= x.
-__device__ __forceinline__ int cta_of(long long x, long long I, long long G)
+// CTA whose tile range holds iteration x: the largest k with range_begin[k] <= x.
+__device__ __forceinline__ int cta_of(int x, const SplitRanges &r)
 {
-    return static_cast<int>(((x + 1) * G + I - 1) / I - 1);
+    int lo = 0, hi = static_cast<int>(gridDim.x) - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (r.begin[mid] <= x)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
 }
 
-__device__ __forceinline__ long long range_begin(long long k, long long I, long long G) { return k * I / G; }
-
-__device__ __forceinline__ bool segment_at(int i, const FwdParams &p, Segment &sg)
+__device__ __forceinline__ bool segment_at(int i, const FwdParams &p, const SplitRanges &r, Segment &sg)
 {
     if (!p.split) {
         const int u = unit_at(i, p.n_units, p.causal);
@@ -227,19 +242,16 @@ __device__ __forceinline__ bool segment_at(int i, const FwdParams &p, Segment &s
         sg.c_first = sg.c_last = static_cast<int>(blockIdx.x);
         return true;
     }
-    const long long I = static_cast<long long>(p.n_units) * p.n_kv;
-    const long long G = gridDim.x;
-    const long long k = blockIdx.x;
-    const long long b = range_begin(k, I, G), e = range_begin(k + 1, I, G);
-    const long long u = b / p.n_kv + i;
+    const int b = r.begin[blockIdx.x], e = r.begin[blockIdx.x + 1];
+    const int u = b / p.n_kv + i;
     if (u * p.n_kv >= e)
         return false;
-    sg.unit = static_cast<int>(u);
-    sg.kv_lo = static_cast<int>(b > u * p.n_kv ? b - u * p.n_kv : 0);
-    sg.kv_hi = static_cast<int>(e < (u + 1) * p.n_kv ? e - u * p.n_kv : p.n_kv);
+    sg.unit = u;
+    sg.kv_lo = b > u * p.n_kv ? b - u * p.n_kv : 0;
+    sg.kv_hi = e < (u + 1) * p.n_kv ? e - u * p.n_kv : p.n_kv;
     sg.slot = i == 0 ? 0 : 1;
-    sg.c_first = cta_of(u * p.n_kv, I, G);
-    sg.c_last = cta_of((u + 1) * p.n_kv - 1, I, G);
+    sg.c_first = cta_of(u * p.n_kv, r);
+    sg.c_last = cta_of((u + 1) * p.n_kv - 1, r);
     return true;
 }
 
@@ -263,7 +275,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *er
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p)
+                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p,
+                   const __grid_constant__ SplitRanges ranges)
 {
     using namespace ptx;
     extern __shared__ uint8_t smem_raw[];
@@ -325,7 +338,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             bool ok = true;
             for (int i = 0; ok; ++i) {
                 Segment sg;
-                if (!segment_at(i, p, sg))
+                if (!segment_at(i, p, ranges, sg))
                     break;
                 int qg, bh;
                 decode_unit(sg.unit, p, qg, bh);
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
         for (int i = 0; ok; ++i) {
             Segment sg;
-            if (!segment_at(i, p, sg))
+            if (!segment_at(i, p, ranges, sg))
                 break;
             int qg, bh;
             decode_unit(sg.unit, p, qg, bh);
@@ -553,7 +566,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
         for (int i = 0; ok; ++i) {
             Segment sg;
-            if (!segment_at(i, p, sg))
+            if (!segment_at(i, p, ranges, sg))
                 break;
             int qg, bh;
             decode_unit(sg.unit, p, qg, bh);
@@ -784,14 +797,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             // summed in CTA order two at a time, so the result does not depend on which
             // CTA merges or on whether its own part comes from TMEM or the workspace.
             auto combine = [&](bool own_from_tmem) {
-                const long long I = static_cast<long long>(p.n_units) * p.n_kv;
-                const long long G = gridDim.x;
                 // The slot of part c: every CTA after the unit's first one starts its
                 // range inside the unit, so the unit is its first segment (slot 0); the
                 // first CTA used slot 0 only if its range starts exactly at the unit's
                 // first tile.
-                const int first_slot =
-                    range_begin(sg.c_first, I, G) == static_cast<long long>(sg.unit) * p.n_kv ? 0 : 1;
+                const int first_slot = ranges.begin[sg.c_first] == sg.unit * p.n_kv ? 0 : 1;
                 auto tile_of = [&](int c) -> size_t {
                     return (static_cast<size_t>(c) * 2 + (c == sg.c_first ? first_slot : 0)) * C::NQ + t;
                 };

@@ -11,6 +11,7 @@
 
 #include "fa2.h"
 #include "fa2_fwd_kernel.cuh"
+#include "fa2_split_ranges.h"
 
 namespace fa2 {
 
@@ -53,30 +54,12 @@ inline WorkspaceLayout workspace_layout(long long G, int NQ, int D)
     return w;
 }
 
-// Grid of the split schedule: one CTA per SM, at most one per K/V-tile iteration.
-inline long long split_grid(long long n_units, long long n_kv, int num_sms)
-{
-    const long long iters = n_units * n_kv;
-    return iters < num_sms ? iters : num_sms;
-}
-
-// Whether cutting the K/V-tile iterations into equal per-SM ranges beats
-// dealing out whole units, in K/V-tile times: whole units finish after
-// ceil(units / SMs) units of n_kv tiles; equal ranges after ceil(units * n_kv
-// / SMs) tiles plus the cost of writing and merging the cut parts (measured on
-// GB300 at about six tile times).  Only taken when it saves at least 5 %.
-inline bool split_pays(long long units, long long n_kv, int num_sms)
-{
-    constexpr long long kPartOverheadTiles = 6;
-    const long long whole = (units + num_sms - 1) / num_sms * n_kv;
-    const long long split = (units * n_kv + num_sms - 1) / num_sms + kPartOverheadTiles;
-    return split * 100 < whole * 95;
-}
-
 enum SplitPolicy { SPLIT_NEVER = 0, SPLIT_AUTO = 1, SPLIT_ALWAYS = 2 };
 
 inline bool use_split(int policy, long long units, long long n_kv, int num_sms)
 {
+    if (units * n_kv > INT_MAX)
+        return false;
     return policy == SPLIT_ALWAYS || (policy == SPLIT_AUTO && split_pays(units, n_kv, num_sms));
 }
 
@@ -142,11 +125,13 @@ fa2_status launch_fwd(const LaunchArgs &a)
     // non-causal passes with a workspace cut the tile iterations into equal ranges
     p.split = (!a.causal && a.workspace != nullptr && use_split(a.split_policy, units, p.n_kv, a.num_sms)) ? 1 : 0;
     long long grid = units < a.num_sms ? units : a.num_sms;
+    SplitRanges ranges{};
     p.counters = nullptr;
     p.part_lse = nullptr;
     p.part_o = nullptr;
     if (p.split) {
-        grid = split_grid(units, p.n_kv, a.num_sms);
+        grid = cut_ranges(units, p.n_kv, static_cast<int>(split_grid(units, p.n_kv, a.num_sms)), ranges.begin,
+                          nullptr);
         const WorkspaceLayout w = workspace_layout(grid, C::NQ, C::D);
         if (a.workspace_bytes < w.total)
             return FA2_ERR_INVALID_ARG;
@@ -167,7 +152,7 @@ fa2_status launch_fwd(const LaunchArgs &a)
         }
         configured.fetch_or(bit);
     }
-    fa2_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+    fa2_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p, ranges);
     return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 

@@ -126,17 +126,18 @@ def test_split_schedule_deterministic_and_reusable(D, split_always):
 
 def test_split_cost_model(monkeypatch):
     """The default estimate takes the cut ranges for one long head (4 query tiles on
-    152+ SMs) and not for many short heads; FA2_SPLIT=never/always override it."""
+    152+ SMs) and not for many short heads (256 units of 8 key tiles);
+    FA2_SPLIT=never/always override it."""
     from io_aware_exact_fa2_gb300 import fa2_workspace_size
     monkeypatch.delenv("FA2_SPLIT", raising=False)
     assert fa2_workspace_size(1, 1, 1000, 4096, 128, False) > 0
-    assert fa2_workspace_size(8, 20, 300, 457, 128, False) == 0
+    assert fa2_workspace_size(4, 16, 1024, 1024, 128, False) == 0
     assert fa2_workspace_size(1, 1, 1000, 4096, 128, True) == 0
     monkeypatch.setenv("FA2_SPLIT", "never")
     assert fa2_workspace_size(1, 1, 1000, 4096, 128, False) == 0
     monkeypatch.setenv("FA2_SPLIT", "always")
-    assert fa2_workspace_size(8, 20, 300, 457, 128, False) > 0
-    assert fa2_workspace_size(8, 20, 300, 457, 128, True) == 0
+    assert fa2_workspace_size(4, 16, 1024, 1024, 128, False) > 0
+    assert fa2_workspace_size(4, 16, 1024, 1024, 128, True) == 0
 
 
 def test_lq_zero_is_a_noop():
