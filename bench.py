@@ -319,7 +319,7 @@ def run_ours(args, world, rank, local):
         per_mode["causal" if c else "noncausal"] = {
             "ms": ms, "tflops": w.flops(c) / (ms * 1e-3) / 1e12,
             "frac_of_peak": w.flops(c) / (ms * 1e-3) / 1e12 / peak,
-            "schedule": ("equal key-tile ranges per SM (fa2_fwd_ws, workspace %d B)" % workspaces[i].numel()
+            "schedule": ("cost-balanced key-tile ranges per SM (fa2_fwd_ws, workspace %d B)" % workspaces[i].numel()
                          if workspaces[i] is not None else "whole query tiles (fa2_fwd)")}
     cpu_val, cpu_desc, cpu_threads, _ = (oracle_sample_run(w, args.cpu_budget)
                                         if (world == 1 and not args.no_cpu_baseline) else (None, "", 0, 0))

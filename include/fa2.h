@@ -99,7 +99,8 @@ fa2_status fa2_workspace_size(int B, int H, int Lq, int Lk, int D, int causal,
 /*
  * fa2_fwd_ws -- fa2_fwd with a caller-owned device workspace, which lets a
  * non-causal pass balance the work evenly over the SMs: the key-tile
- * iterations of all query tiles are cut into one equal range per SM, and a
+ * iterations of all query tiles are cut into one range per SM, the ranges
+ * balanced in tiles plus a fixed cost per query tile they touch, and a
  * query tile whose keys straddle two ranges is computed in parts that are
  * merged afterwards: each part's O and log-sum-exp are combined exactly as
  * the online softmax merges two key blocks (Olowookere, "FlashAttention-2
