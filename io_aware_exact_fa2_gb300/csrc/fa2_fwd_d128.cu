@@ -9,7 +9,7 @@
 namespace fa2 {
 
 // Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row,
-// S buffers per Q tile);
+// S buffers per Q tile, Q kept in TMEM);
 // overridable at compile time for tuning sweeps.
 #ifndef FA2_D128_BN
 #define FA2_D128_BN 128
@@ -23,11 +23,15 @@ namespace fa2 {
 #ifndef FA2_D128_NS
 #define FA2_D128_NS (FA2_D128_NQ == 1 ? 2 : 1)
 #endif
+#ifndef FA2_D128_QT
+#define FA2_D128_QT 0
+#endif
 #ifndef FA2_D128_CS
 #define FA2_D128_CS 1
 #endif
 
-using CfgD128 = FwdCfg<128, FA2_D128_BN, FA2_D128_NQ, FA2_D128_KS, FA2_D128_CS, FA2_D128_NS>;
+using CfgD128 = FwdCfg<128, FA2_D128_BN, FA2_D128_NQ, FA2_D128_KS, FA2_D128_CS, FA2_D128_NS,
+                      FA2_D128_QT>;
 
 fa2_status launch_fwd_d128(const LaunchArgs &a) { return launch_fwd<CfgD128>(a); }
 

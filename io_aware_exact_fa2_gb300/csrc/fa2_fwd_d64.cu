@@ -9,7 +9,7 @@
 namespace fa2 {
 
 // Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row,
-// S buffers per Q tile);
+// S buffers per Q tile, Q kept in TMEM);
 // overridable at compile time for tuning sweeps.
 #ifndef FA2_D64_BN
 #define FA2_D64_BN 128
@@ -23,11 +23,15 @@ namespace fa2 {
 #ifndef FA2_D64_NS
 #define FA2_D64_NS (FA2_D64_NQ == 1 ? 2 : 1)
 #endif
+#ifndef FA2_D64_QT
+#define FA2_D64_QT 0
+#endif
 #ifndef FA2_D64_CS
 #define FA2_D64_CS 1
 #endif
 
-using CfgD64 = FwdCfg<64, FA2_D64_BN, FA2_D64_NQ, FA2_D64_KS, FA2_D64_CS, FA2_D64_NS>;
+using CfgD64 = FwdCfg<64, FA2_D64_BN, FA2_D64_NQ, FA2_D64_KS, FA2_D64_CS, FA2_D64_NS,
+                      FA2_D64_QT>;
 
 fa2_status launch_fwd_d64(const LaunchArgs &a) { return launch_fwd<CfgD64>(a); }
 

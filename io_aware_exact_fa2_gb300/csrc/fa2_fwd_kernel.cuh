@@ -88,7 +88,7 @@ enum : int {
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.69314718055994530942f;
 
-template <int D_, int BN_, int NQ_, int KS_, int CS_, int NS_ = (NQ_ == 1 ? 2 : 1)>
+template <int D_, int BN_, int NQ_, int KS_, int CS_, int NS_ = (NQ_ == 1 ? 2 : 1), int QT_ = 0>
 struct FwdCfg {
     static constexpr int D = D_;     // head dimension
     static constexpr int BN = BN_;   // K/V rows per tile
@@ -97,6 +97,9 @@ struct FwdCfg {
     static constexpr int CS = CS_;   // softmax warps sharing one row (column split)
     static constexpr int BM = 128;   // Q rows per tile = TMEM lanes = MMA M
     static constexpr int NS = NS_;                // S/P TMEM buffers per Q tile
+    // QT: Q lives in TMEM and S = Q K^T takes A from TMEM; the softmax warps copy each
+    // Q tile there from shared memory.  Needs one Q tile per unit (TMEM budget).
+    static constexpr bool QT = QT_ != 0;
     static constexpr int NCOL = BN / CS;          // S columns per softmax thread
     static constexpr int OCOL = D / CS;           // O columns per softmax thread
     static constexpr int DB = D / 64;             // 64-column (128-byte) swizzle blocks
@@ -126,14 +129,20 @@ struct FwdCfg {
     static constexpr int BAR_XMAX = BAR_O_FREE + NQ;         // [NQ][2]
     static constexpr int BAR_GROUP = BAR_XMAX + 2 * NQ;      // [NQ]
     static constexpr int BAR_DRAIN = BAR_GROUP + NQ;
-    static constexpr int NUM_BARS = BAR_DRAIN + 1;
+    static constexpr int BAR_QT_FULL = BAR_DRAIN + 1;        // [2] Q copied into TMEM buffer
+    static constexpr int BAR_QT_EMPTY = BAR_QT_FULL + 2;     // [2] last S MMA read the buffer
+    static constexpr int NUM_BARS = BAR_QT_EMPTY + 2;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;  // + slack for base alignment
 
     // tensor memory columns
     static constexpr int TM_O = 0;        // O of tile t: columns [t*D, (t+1)*D)
     static constexpr int TM_S = NQ * D;   // S/P buffer (t, b): TM_S + (t*NS + b)*BN
-    static constexpr int TMEM_USED = NQ * D + NQ * NS * BN;
+    static constexpr int TM_Q = NQ * D + NQ * NS * BN;   // QT: Q buffer q at TM_Q + q*D/2
+    // Q buffers in TMEM: two where they fit (segments alternate), else one, which the
+    // next segment's copy reuses once the current segment's last S has read it
+    static constexpr int QB = (TM_Q + D <= 512) ? 2 : 1;
+    static constexpr int TMEM_USED = TM_Q + (QT ? QB * D / 2 : 0);
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
                                    : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
 
@@ -163,6 +172,8 @@ struct FwdCfg {
     static_assert(NS == 1 || NS == 2, "one or two S buffers per Q tile");
     static_assert(NCOL % 32 == 0 && OCOL % 32 == 0, "per-thread column slices are whole 32-column loads");
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
+    static_assert(!QT || NQ == 1, "Q in TMEM needs one Q tile per unit");
+    static_assert(!QT || (D / CS) % 64 == 0, "Q copy works on whole 64-column swizzle blocks");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
 
@@ -290,7 +301,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int t = 0; t < C::NQ; ++t) {
             mbar_init(bar(C::BAR_Q_FULL + t), 1);
-            mbar_init(bar(C::BAR_Q_EMPTY + t), 1);
+            // with Q in TMEM the softmax threads free the shared-memory copy once copied
+            mbar_init(bar(C::BAR_Q_EMPTY + t), C::QT ? C::GROUP_THREADS : 1);
             mbar_init(bar(C::BAR_O_DONE + t), 1);
             mbar_init(bar(C::BAR_O_FREE + t), C::GROUP_THREADS);
             mbar_init(bar(C::BAR_XMAX + 2 * t), C::GROUP_THREADS);
@@ -308,6 +320,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_init(bar(C::BAR_P_READY + i), C::GROUP_THREADS);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(bar(C::BAR_QT_FULL + q), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_QT_EMPTY + q), 1);
+        }
         fence_mbar_init();
     }
     if (warp == C::WARP_MMA) {
@@ -435,6 +451,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 n_t[t] = segment_tiles(sg, q0 + t * C::BM, p, C::BN);
                 n_max = max(n_max, n_t[t]);
             }
+            // QT: the TMEM buffer holding this segment's Q (segments alternate)
+            const uint32_t qt_buf = q_loads[0] % C::QB;
             // the last Q tile (highest t) that reads K/V tile j
             auto last_user = [&](int j) {
                 int lu = 0;
@@ -456,18 +474,28 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const int b = g % C::NS;
                 if (leader) {
                     const uint32_t d = tmem + C::TM_S + (t * C::NS + b) * C::BN;
-                    const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
                     const uint64_t dk = desc_k + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
+                    if constexpr (C::QT) {
+                        // A = Q from TMEM buffer qt_buf: 16 bf16 (8 columns) per K step
+                        const uint32_t a = tmem + C::TM_Q + qt_buf * (C::D / 2);
 #pragma unroll
-                    for (int kk = 0; kk < C::D / 16; ++kk)
-                        mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
-                               dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
-                               C::IDESC_S, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < C::D / 16; ++kk)
+                            mma_ts(d, a + kk * 8,
+                                   dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
+                                   C::IDESC_S, kk > 0 ? 1u : 0u);
+                    } else {
+                        const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < C::D / 16; ++kk)
+                            mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
+                                   dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
+                                   C::IDESC_S, kk > 0 ? 1u : 0u);
+                    }
                     mma_commit(bar(C::BAR_S_FULL + t * C::NS + b));
                     if (last_user(j) == t)
                         mma_commit(bar(C::BAR_K_EMPTY + s));
-                    if (j == n_t[t] - 1)
-                        mma_commit(bar(C::BAR_Q_EMPTY + t));   // last read of this unit's Q tile
+                    if (j == n_t[t] - 1)   // last read of this unit's Q tile
+                        mma_commit(bar(C::QT ? C::BAR_QT_EMPTY + qt_buf : C::BAR_Q_EMPTY + t));
                 }
                 __syncwarp();
                 return true;
@@ -505,11 +533,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 return true;
             };
 
-            // this unit's Q tiles
+            // this unit's Q tiles: in shared memory (TMA), or copied into TMEM buffer
+            // qt_buf by the softmax warps
 #pragma unroll
             for (int t = 0; t < C::NQ; ++t) {
                 if (ok && n_t[t] > 0) {
-                    ok = warp_wait(bar(C::BAR_Q_FULL + t), q_loads[t] & 1, p.err, ERR_MMA | 1, p.wait_limit_ns);
+                    if constexpr (C::QT)
+                        ok = warp_wait(bar(C::BAR_QT_FULL + qt_buf), (q_loads[0] / C::QB) & 1, p.err,
+                                       ERR_MMA | 6, p.wait_limit_ns);
+                    else
+                        ok = warp_wait(bar(C::BAR_Q_FULL + t), q_loads[t] & 1, p.err, ERR_MMA | 1,
+                                       p.wait_limit_ns);
                     ++q_loads[t];
                 }
             }
@@ -563,6 +597,36 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         uint32_t tbase = 0;    // S tiles of this slot in earlier segments (running phase base)
         uint32_t group_uses = 0;   // completed phases of this slot's group barrier
         bool ok = true;
+        // QT: copy the next Q tile from shared memory into TMEM buffer (q_copies % QB).
+        // Each thread moves its own row's slice of D/CS columns: 16-byte pieces of the
+        // 128B-swizzled rows (piece c of row r sits at c ^ (r % 8)) become packed bf16
+        // pairs, two per TMEM column, as the MMA's A operand expects.
+        uint32_t q_copies = 0;
+        auto copy_q = [&]() -> bool {
+            const uint32_t qb = q_copies % C::QB;
+            if (!warp_wait(bar(C::BAR_Q_FULL), q_copies & 1, p.err, ERR_SOFTMAX | 8, p.wait_limit_ns))
+                return false;
+            // the segment that used this buffer before (QB copies ago) has issued its last S
+            if (q_copies >= C::QB && !warp_wait(bar(C::BAR_QT_EMPTY + qb), (q_copies / C::QB - 1) & 1, p.err,
+                                                ERR_SOFTMAX | 9, p.wait_limit_ns))
+                return false;
+            tc_fence_after();
+#pragma unroll
+            for (int bq = h * (C::OCOL / 64); bq < (h + 1) * (C::OCOL / 64); ++bq) {
+                const uint32_t src = sbase + C::OFF_Q + bq * C::Q_BLOCK + row * 128;
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    ld_shared_v4(src + ((c ^ (row & 7)) * 16), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                tmem_st32(tmem + lane_base + C::TM_Q + qb * (C::D / 2) + bq * 32, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar(C::BAR_QT_FULL + qb));
+            mbar_arrive(bar(C::BAR_Q_EMPTY));
+            ++q_copies;
+            return true;
+        };
 
         for (int i = 0; ok; ++i) {
             Segment sg;
@@ -576,6 +640,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (n == 0)
                 continue;
             const int kv0 = p.split ? sg.kv_lo : 0;  // absolute index of the segment's first K/V tile
+            if constexpr (C::QT) {
+                if (i == 0 && !(ok = copy_q()))
+                    break;
+            }
             float m_use = -INFINITY;   // running max (log2 domain, possibly stale by < 2^THRESHOLD)
             float l = 0.f;             // running normaliser of the fp32 weights (for LSE)
             float l_o = 0.f;           // running normaliser of the bf16 weights the PV MMA sees (for O)
@@ -744,6 +812,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             if (!ok)
                 break;
+            if constexpr (C::QT) {
+                // the next segment's Q goes into TMEM now, so its first S MMAs run during
+                // this epilogue
+                Segment next;
+                if (segment_at(i + 1, p, ranges, next) && !(ok = copy_q()))
+                    break;
+            }
 
             // ---- epilogue: O out of TMEM (then released to the MMA warp), O / l -> bf16
             // rows and LSE straight to global memory; a cut unit's part goes to the
