@@ -167,16 +167,24 @@ fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
 
 /*
  * fa2_fwd_from_host -- the same pass starting from, and ending in, HOST
- * memory: enqueues on `stream` the host->device copies of q, k, v into the
- * caller's device staging buffers, the kernel, and the device->host copies of
- * O and LSE back into the caller's host buffers.  Host buffers should be
- * pinned (page-locked) for the copies to be asynchronous.  The caller must
- * synchronise `stream` before reading o_host / lse_host.
+ * memory: copies q, k, v from the host into the caller's device staging
+ * buffers, runs the pass, and copies O and LSE back into the caller's host
+ * buffers.  Host buffers should be pinned (page-locked) for the copies to be
+ * asynchronous.
+ *
+ * The work is cut into up to 8 chunks of whole heads and overlapped: chunk c's
+ * kernel runs while chunk c+1's inputs arrive and chunk c-1's outputs leave.
+ * Copies and kernels run on three streams of the library's own (per device,
+ * created by the first call), ordered after all work already enqueued on
+ * `stream`, and `stream` waits for them: once `stream` has been synchronised,
+ * o_host and lse_host hold the results.  Calls from several host threads
+ * enqueue one at a time.
  *
  *   q_host .. lse_host   host pointers (same layouts as fa2_fwd).
  *   q_dev  .. lse_dev    caller-owned device buffers of the same sizes.
  *
- * Errors: as fa2_fwd; FA2_ERR_CUDA if a copy cannot be enqueued.
+ * Errors: as fa2_fwd; FA2_ERR_CUDA if a copy cannot be enqueued or the
+ * library's streams cannot be created.
  */
 fa2_status fa2_fwd_from_host(const void *q_host, const void *k_host,
                              const void *v_host, void *o_host, float *lse_host,

@@ -155,9 +155,10 @@ def fa2_fwd_noalloc(q, k, v, o, lse, causal: bool, scale: float | None = None, s
 
 def fa2_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,
                       causal: bool, scale: float | None = None, stream=None) -> None:
-    """Host buffers in, host buffers out (copies and kernel enqueued on `stream`).
+    """Host buffers in, host buffers out: copies and kernels overlapped over chunks of
+    heads on the library's own streams, ordered after `stream`'s earlier work.
 
-    The caller synchronises the stream before reading o_host / lse_host.
+    The caller synchronises `stream` before reading o_host / lse_host.
     """
     B, H, Lq, Lk, D = _check_shapes(q_host, k_host, v_host, o_host, lse_host)
     _check_shapes(q_dev, k_dev, v_dev, o_dev, lse_dev)

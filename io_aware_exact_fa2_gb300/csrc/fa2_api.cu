@@ -109,6 +109,44 @@ int *device_error_ptr(int dev)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// Streams and events with which fa2_fwd_from_host overlaps its host->device copies,
+// kernels and device->host copies across chunks of heads: one stream per kind of
+// work, so chunk c's kernel runs while chunk c+1's inputs arrive and chunk c-1's
+// outputs leave.  One set per device, created on first use with the device current.
+struct HostPipe {
+    static constexpr int kChunks = 8;
+    cudaStream_t h2d = nullptr, compute = nullptr, d2h = nullptr;
+    cudaEvent_t entry = nullptr, exit = nullptr;
+    cudaEvent_t inputs[kChunks] = {}, outputs[kChunks] = {};
+    std::mutex mu;   // one call at a time enqueues (the events are shared)
+    bool ok = false;
+};
+
+HostPipe *host_pipe(int dev)
+{
+    static std::mutex mu;
+    static HostPipe *pipes[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pipes[dev]) {
+        HostPipe *hp = new HostPipe;
+        bool ok = cudaStreamCreateWithFlags(&hp->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&hp->compute, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp->entry, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp->exit, cudaEventDisableTiming) == cudaSuccess;
+        for (int c = 0; ok && c < HostPipe::kChunks; ++c)
+            ok = cudaEventCreateWithFlags(&hp->inputs[c], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp->outputs[c], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok)
+            (void)cudaGetLastError();
+        hp->ok = ok;
+        pipes[dev] = hp;
+    }
+    return pipes[dev]->ok ? pipes[dev] : nullptr;
+}
+
 // Pure host-side checks (no CUDA call).
 fa2_status validate(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int H,
                     int Lq, int Lk, int D, float scale)
@@ -290,25 +328,64 @@ FA2_EXPORT fa2_status fa2_fwd_from_host(const void *q_host, const void *k_host, 
     st = fa2::select_device_of(q_dev, &dev);
     if (st != FA2_OK)
         return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t bh = static_cast<size_t>(B) * static_cast<size_t>(H);
-    const size_t q_bytes = bh * static_cast<size_t>(Lq) * D * 2;
-    const size_t kv_bytes = bh * static_cast<size_t>(Lk) * D * 2;
-    const size_t lse_bytes = bh * static_cast<size_t>(Lq) * sizeof(float);
-    if (cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(k_dev, k_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(v_dev, v_host, kv_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    fa2::HostPipe *hp = fa2::host_pipe(dev);
+    if (!hp)
+        return FA2_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int bh = B * H;   // validated: fits an int
+    const size_t q_head = static_cast<size_t>(Lq) * D * 2, kv_head = static_cast<size_t>(Lk) * D * 2;
+    const size_t lse_head = static_cast<size_t>(Lq) * sizeof(float);
+    // chunks of whole heads, each moving at least ~4 MB in, so that copy set-up
+    // costs stay small against the transfer
+    const size_t in_bytes = static_cast<size_t>(bh) * (q_head + 2 * kv_head);
+    int chunks = static_cast<int>(in_bytes / (size_t{4} << 20));
+    chunks = chunks < 1 ? 1 : chunks > fa2::HostPipe::kChunks ? fa2::HostPipe::kChunks : chunks;
+    chunks = chunks > bh ? bh : chunks;
+
+    std::lock_guard<std::mutex> lock(hp->mu);
+    auto fail = [] {
         (void)cudaGetLastError();
         return FA2_ERR_CUDA;
+    };
+    // everything below runs after the work already on `stream`
+    if (cudaEventRecord(hp->entry, s) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->entry, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->compute, hp->entry, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->d2h, hp->entry, 0) != cudaSuccess)
+        return fail();
+    char *qd = static_cast<char *>(q_dev), *kd = static_cast<char *>(k_dev), *vd = static_cast<char *>(v_dev);
+    char *od = static_cast<char *>(o_dev), *ld = reinterpret_cast<char *>(lse_dev);
+    const char *qh = static_cast<const char *>(q_host), *kh = static_cast<const char *>(k_host);
+    const char *vh = static_cast<const char *>(v_host);
+    char *oh = static_cast<char *>(o_host), *lh = reinterpret_cast<char *>(lse_host);
+    for (int c = 0; c < chunks; ++c) {
+        const size_t h0 = static_cast<size_t>(bh) * c / chunks, h1 = static_cast<size_t>(bh) * (c + 1) / chunks;
+        const size_t nh = h1 - h0;
+        if (cudaMemcpyAsync(qd + h0 * q_head, qh + h0 * q_head, nh * q_head, cudaMemcpyHostToDevice, hp->h2d) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(kd + h0 * kv_head, kh + h0 * kv_head, nh * kv_head, cudaMemcpyHostToDevice, hp->h2d) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(vd + h0 * kv_head, vh + h0 * kv_head, nh * kv_head, cudaMemcpyHostToDevice, hp->h2d) !=
+                cudaSuccess ||
+            cudaEventRecord(hp->inputs[c], hp->h2d) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->compute, hp->inputs[c], 0) != cudaSuccess)
+            return fail();
+        st = fa2::launch(qd + h0 * q_head, kd + h0 * kv_head, vd + h0 * kv_head, od + h0 * q_head,
+                         reinterpret_cast<float *>(ld + h0 * lse_head), 1, static_cast<int>(nh), Lq, Lk, D, causal,
+                         scale, hp->compute);
+        if (st != FA2_OK)
+            return st;
+        if (cudaEventRecord(hp->outputs[c], hp->compute) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->d2h, hp->outputs[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync(oh + h0 * q_head, od + h0 * q_head, nh * q_head, cudaMemcpyDeviceToHost, hp->d2h) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(lh + h0 * lse_head, ld + h0 * lse_head, nh * lse_head, cudaMemcpyDeviceToHost,
+                            hp->d2h) != cudaSuccess)
+            return fail();
     }
-    st = fa2::launch(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, Lq, Lk, D, causal, scale, s);
-    if (st != FA2_OK)
-        return st;
-    if (cudaMemcpyAsync(o_host, o_dev, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(lse_host, lse_dev, lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return FA2_ERR_CUDA;
-    }
+    // `stream` continues once the last outputs are on the host (the d2h stream's
+    // work follows every kernel, and every kernel follows its inputs)
+    if (cudaEventRecord(hp->exit, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(s, hp->exit, 0) != cudaSuccess)
+        return fail();
     return FA2_OK;
 }
 
