@@ -149,6 +149,9 @@ struct FwdCfg {
     // warp roles: softmax warpgroups first, then a control warpgroup (TMA
     // producer warp, MMA warp and, when registers are re-split, two idle warps)
     static constexpr int GROUP_THREADS = 128 * CS;             // softmax threads per Q tile
+    // Barriers the softmax warps signal take one arrival per warp (after a __syncwarp),
+    // not one per thread: 32x fewer shared-memory atomics on every step's P_READY.
+    static constexpr int GROUP_WARPS = GROUP_THREADS / 32;
     static constexpr int NUM_SOFTMAX_WARPS = 4 * CS * NQ;
     static constexpr int WARP_PRODUCER = NUM_SOFTMAX_WARPS;
     static constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;
@@ -302,12 +305,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         for (int t = 0; t < C::NQ; ++t) {
             mbar_init(bar(C::BAR_Q_FULL + t), 1);
             // with Q in TMEM the softmax threads free the shared-memory copy once copied
-            mbar_init(bar(C::BAR_Q_EMPTY + t), C::QT ? C::GROUP_THREADS : 1);
+            mbar_init(bar(C::BAR_Q_EMPTY + t), C::QT ? C::GROUP_WARPS : 1);
             mbar_init(bar(C::BAR_O_DONE + t), 1);
-            mbar_init(bar(C::BAR_O_FREE + t), C::GROUP_THREADS);
-            mbar_init(bar(C::BAR_XMAX + 2 * t), C::GROUP_THREADS);
-            mbar_init(bar(C::BAR_XMAX + 2 * t + 1), C::GROUP_THREADS);
-            mbar_init(bar(C::BAR_GROUP + t), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_O_FREE + t), C::GROUP_WARPS);
+            mbar_init(bar(C::BAR_XMAX + 2 * t), C::GROUP_WARPS);
+            mbar_init(bar(C::BAR_XMAX + 2 * t + 1), C::GROUP_WARPS);
+            mbar_init(bar(C::BAR_GROUP + t), C::GROUP_WARPS);
         }
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(bar(C::BAR_K_FULL + s), 1);
@@ -317,11 +320,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         for (int i = 0; i < C::NQ * C::NS; ++i) {
             mbar_init(bar(C::BAR_S_FULL + i), 1);
-            mbar_init(bar(C::BAR_P_READY + i), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_P_READY + i), C::GROUP_WARPS);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
         for (int q = 0; q < 2; ++q) {
-            mbar_init(bar(C::BAR_QT_FULL + q), C::GROUP_THREADS);
+            mbar_init(bar(C::BAR_QT_FULL + q), C::GROUP_WARPS);
             mbar_init(bar(C::BAR_QT_EMPTY + q), 1);
         }
         fence_mbar_init();
@@ -594,6 +597,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const uint32_t xmax = sbase + C::OFF_XMAX + t * (2 * C::CS * 128 * 4);
         const uint32_t xl = sbase + C::OFF_XL + t * (C::CS * 128 * 8);
         const float c2 = p.scale_log2;
+        // one arrival per warp: every lane's prior writes (shared memory, and TMEM
+        // after its own wait + fence) are ordered before lane 0's arrive by the
+        // __syncwarp, and the arrive releases them to the waiting side
+        auto warp_arrive = [&](uint32_t b) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b);
+        };
         uint32_t tbase = 0;    // S tiles of this slot in earlier segments (running phase base)
         uint32_t group_uses = 0;   // completed phases of this slot's group barrier
         bool ok = true;
@@ -622,8 +633,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bar(C::BAR_QT_FULL + qb));
-            mbar_arrive(bar(C::BAR_Q_EMPTY));
+            warp_arrive(bar(C::BAR_QT_FULL + qb));
+            warp_arrive(bar(C::BAR_Q_EMPTY));
             ++q_copies;
             return true;
         };
@@ -701,7 +712,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 if constexpr (C::CS > 1) {
                     const uint32_t xb = xmax + (g & 1) * (C::CS * 128 * 4);
                     st_shared_f32(xb + (h * 128 + row) * 4, mx);
-                    mbar_arrive(bar(C::BAR_XMAX + 2 * t + (g & 1)));
+                    warp_arrive(bar(C::BAR_XMAX + 2 * t + (g & 1)));
                     ok = warp_wait(bar(C::BAR_XMAX + 2 * t + (g & 1)), (g >> 1) & 1, p.err, ERR_SOFTMAX | 4,
                                    p.wait_limit_ns);
                     if (!ok)
@@ -808,7 +819,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 // P_READY is per S buffer: the softmax may finish tile j+1 before the MMA
                 // warp has seen tile j, but it can only reuse a buffer after the MMA warp
                 // issued the S that refills it, i.e. after it consumed that buffer's P.
-                mbar_arrive(bar(C::BAR_P_READY + t * C::NS + b));
+                warp_arrive(bar(C::BAR_P_READY + t * C::NS + b));
             }
             if (!ok)
                 break;
@@ -829,7 +840,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 break;
             // all threads of this slot's group arrive, then wait for the phase to complete
             auto group_sync = [&](int code) -> bool {
-                mbar_arrive(bar(C::BAR_GROUP + t));
+                warp_arrive(bar(C::BAR_GROUP + t));
                 const bool r = warp_wait(bar(C::BAR_GROUP + t), group_uses & 1, p.err, ERR_SOFTMAX | code,
                                          p.wait_limit_ns);
                 ++group_uses;
@@ -907,7 +918,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         tmem_ld_wait(r);
                         if (cc == C::OCOL / 32 - 1) {
                             tc_fence_before();
-                            mbar_arrive(bar(C::BAR_O_FREE + t));
+                            warp_arrive(bar(C::BAR_O_FREE + t));
                         }
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
@@ -995,7 +1006,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     if (cc == C::OCOL / 32 - 1) {
                         // every read of O_t is done: the next segment's first PV may overwrite it
                         tc_fence_before();
-                        mbar_arrive(bar(C::BAR_O_FREE + t));
+                        warp_arrive(bar(C::BAR_O_FREE + t));
                     }
                     if (whole) {
                         uint32_t w[16];
