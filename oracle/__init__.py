@@ -15,8 +15,14 @@ as stated in Olowookere, "FlashAttention-2 from scratch with a custom Triton
 kernel" (section "The core idea: making attention IO-aware") and "Chapter 08:
 Flash Attention -- blocked attention" (sections 3 and 4).
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms,
-invariants, brute force, a library cross-check); none is "parity unpinned".
+It also holds the backward definition of the same attention (Chapter 08,
+section 6: Delta, the softmax backward, dV = P^T dO, dK = scale dS^T Q,
+dQ = scale dS K) and an fp64-input forward for numerical differentiation.
+
+Every function here is pinned: the forward by ``tests/test_oracle_pins.py``
+(closed forms, invariants, brute force, a library cross-check), the gradients
+by ``tests/test_oracle_grad_pins.py`` (finite differences of the forward,
+torch autograd, invariants, a closed form); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -67,6 +73,13 @@ def _load():
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
             lib.fa2_oracle_max_threads.restype = ctypes.c_int
             lib.fa2_oracle_max_threads.argtypes = []
+            i64, vp = ctypes.c_int64, ctypes.c_void_p
+            lib.fa2_oracle_fwd_f64.restype = ctypes.c_int
+            lib.fa2_oracle_fwd_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int,
+                                               ctypes.c_double, vp, vp, ctypes.c_int]
+            lib.fa2_oracle_bwd_f64.restype = ctypes.c_int
+            lib.fa2_oracle_bwd_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int,
+                                               ctypes.c_double, vp, vp, vp, vp, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -128,3 +141,65 @@ def attention(q, k, v, causal: bool, scale: float, threads: int = 0):
     B, H, Lq, D = q.shape
     o, lse = attention_rows(q, k, v, causal, scale, None, False, threads)
     return o.reshape(B, H, Lq, D), lse.reshape(B, H, Lq)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def forward_f64(q, k, v, causal: bool, scale: float, threads: int = 0):
+    """Forward definition on fp64 arrays (B, H, L, D): (O fp64 (B, H, Lq, D), LSE (B, H, Lq)).
+
+    The same per-row arithmetic as ``attention`` without the bf16 widening, so a
+    test can perturb the inputs by amounts bf16 cannot hold.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    o = np.empty((B, H, Lq, D))
+    lse = np.empty((B, H, Lq))
+    rc = _load().fa2_oracle_fwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Lq, Lk, D,
+                                     int(bool(causal)), float(scale), o.ctypes.data, lse.ctypes.data, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"fa2_oracle_fwd_f64 failed with code {rc}")
+    return o, lse
+
+
+def gradients_f64(q, k, v, do, causal: bool, scale: float, threads: int = 0):
+    """Backward definition on fp64 arrays: (dQ, dK, dV, Delta) for L with dL/dO = do.
+
+    Chapter 08, section 6: Delta = rowsum(dO * O), dS = P * (dO V^T - Delta),
+    dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K (see fa2_oracle.c).
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    dq = np.empty((B, H, Lq, D))
+    dk = np.empty((B, H, Lk, D))
+    dv = np.empty((B, H, Lk, D))
+    delta = np.empty((B, H, Lq))
+    rc = _load().fa2_oracle_bwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, do.ctypes.data, B, H, Lq, Lk, D,
+                                     int(bool(causal)), float(scale), dq.ctypes.data, dk.ctypes.data,
+                                     dv.ctypes.data, delta.ctypes.data, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"fa2_oracle_bwd_f64 failed with code {rc}")
+    return dq, dk, dv, delta
+
+
+def gradients(q, k, v, do, causal: bool, scale: float, heads=None, threads: int = 0):
+    """Backward definition for bf16 inputs (torch tensors, widened exactly to fp64).
+
+    heads: optional list of flat head ids b*H + h to compute (default: all); the
+    results then have shape (len(heads), L, D).  Returns (dQ, dK, dV, Delta) fp64.
+    """
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    arrs = [decode_bf16(_bf16_bits(t)).reshape(B * H, t.shape[2], D) for t in (q, k, v, do)]
+    if heads is not None:
+        idx = np.asarray(heads, dtype=np.int64)
+        arrs = [a[idx] for a in arrs]
+    n = arrs[0].shape[0]
+    dq, dk, dv, delta = gradients_f64(*(a.reshape(1, n, a.shape[1], D) for a in arrs), causal, scale, threads)
+    if heads is None:
+        return (dq.reshape(B, H, Lq, D), dk.reshape(B, H, Lk, D), dv.reshape(B, H, Lk, D), delta.reshape(B, H, Lq))
+    return dq[0], dk[0], dv[0], delta[0]

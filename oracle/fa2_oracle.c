@@ -185,6 +185,206 @@ int fa2_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     return failed ? 2 : 0;
 }
 
+/*
+ * ------------------------------------------------------------------ gradients
+ *
+ * The backward pass of the same attention ("Chapter 08: Flash Attention --
+ * blocked attention", section 6: 6.2 the per-row scalar Delta, 6.3 the softmax
+ * backward, 6.4 the three gradient lines).  Given the upstream gradient dO of a
+ * loss L with respect to O, the gradients of L with respect to the inputs are,
+ * per (b, h), with P the materialised probabilities of the forward definition:
+ *
+ *   Delta_i = sum_d dO_id * O_id                       (one scalar per query row)
+ *   dP_ij   = sum_d dO_id * V_jd                       (dP = dO V^T)
+ *   dS_ij   = P_ij * (dP_ij - Delta_i)                 (softmax backward; dS is the
+ *                                                       gradient of the scaled score)
+ *   dV_jd   = sum_i P_ij * dO_id                       (dV = P^T dO)
+ *   dK_jd   = scale * sum_i dS_ij * Q_id               (dK = scale * dS^T Q)
+ *   dQ_id   = scale * sum_j dS_ij * K_jd               (dQ = scale * dS K)
+ *
+ * Masked positions have P_ij = 0 and so contribute nothing.  The section works
+ * in base 2 (P = 2^(S' - LSE_2) with S' carrying scale * log2 e, hence its ln 2
+ * factors); in natural-log terms with the scale applied to the scores the
+ * factors cancel into the plain expressions above.
+ *
+ * Per query row the oracle materialises the full P row (through one_row, the
+ * forward definition), the full dP row and the full dS row in fp64 before
+ * using them, and accumulates dK, dV over the rows in row order (one head per
+ * thread, so the order is fixed).
+ */
+
+/* fp64 forward for fp64 inputs (contiguous (B, H, L, D)); same row definition. */
+static int64_t one_row_f64(const double *q_row, const double *k_head, const double *v_head, int64_t i,
+                           int64_t Lk, int64_t D, int causal, double scale, double *s, double *p,
+                           double *o_row, double *lse_out)
+{
+    int64_t n_allowed = 0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (!allowed(i, j, causal)) {
+            s[j] = -INFINITY;
+            continue;
+        }
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            dot += q_row[d] * k_head[j * D + d];
+        s[j] = scale * dot;
+        if (s[j] > m)
+            m = s[j];
+        ++n_allowed;
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (allowed(i, j, causal)) {
+            p[j] = exp(s[j] - m);
+            z += p[j];
+        } else {
+            p[j] = 0.0;
+        }
+    }
+    for (int64_t j = 0; j < Lk; ++j)
+        p[j] = p[j] / z;
+    for (int64_t d = 0; d < D; ++d)
+        o_row[d] = 0.0;
+    for (int64_t j = 0; j < Lk; ++j) {
+        if (!allowed(i, j, causal))
+            continue;
+        for (int64_t d = 0; d < D; ++d)
+            o_row[d] += p[j] * v_head[j * D + d];
+    }
+    *lse_out = m + log(z);
+    return n_allowed;
+}
+
+/*
+ * Forward for fp64 inputs, every row: o (B, H, Lq, D), lse (B, H, Lq).  Lets a
+ * test differentiate the forward definition numerically.  Returns as
+ * fa2_oracle_rows.
+ */
+int fa2_oracle_fwd_f64(const double *q, const double *k, const double *v, int64_t B, int64_t H, int64_t Lq,
+                       int64_t Lk, int64_t D, int causal, double scale, double *o, double *lse, int n_threads)
+{
+    if (!q || !k || !v || !o || !lse || B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0)
+        return 1;
+    int failed = 0;
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)Lk * sizeof(double));
+        double *p = (double *)malloc((size_t)Lk * sizeof(double));
+        if (!s || !p) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t r = 0; r < B * H * Lq; ++r) {
+                const int64_t bh = r / Lq, i = r % Lq;
+                one_row_f64(q + r * D, k + bh * Lk * D, v + bh * Lk * D, i, Lk, D, causal, scale, s, p,
+                            o + r * D, lse + r);
+            }
+        }
+        free(s);
+        free(p);
+    }
+    return failed ? 2 : 0;
+}
+
+/* Gradients of one head (all fp64); s, p, dp: scratch rows of Lk; o_row: D. */
+static void one_head_bwd(const double *q, const double *k, const double *v, const double *dout, int64_t Lq,
+                         int64_t Lk, int64_t D, int causal, double scale, double *dq, double *dk, double *dv,
+                         double *delta, double *s, double *p, double *dp, double *o_row)
+{
+    for (int64_t t = 0; t < Lk * D; ++t) {
+        dk[t] = 0.0;
+        dv[t] = 0.0;
+    }
+    for (int64_t i = 0; i < Lq; ++i) {
+        const double *q_row = q + i * D, *do_row = dout + i * D;
+        double lse;
+        one_row_f64(q_row, k, v, i, Lk, D, causal, scale, s, p, o_row, &lse);
+        /* Delta_i = dO_i . O_i */
+        double dl = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            dl += do_row[d] * o_row[d];
+        if (delta)
+            delta[i] = dl;
+        /* dP row, then dS row (kept in dp) */
+        for (int64_t j = 0; j < Lk; ++j) {
+            if (!allowed(i, j, causal)) {
+                dp[j] = 0.0;
+                continue;
+            }
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                acc += do_row[d] * v[j * D + d];
+            dp[j] = p[j] * (acc - dl);
+        }
+        /* dQ_i = scale * sum_j dS_ij K_j;  dK_j += scale * dS_ij Q_i;  dV_j += P_ij dO_i */
+        double *dq_row = dq + i * D;
+        for (int64_t d = 0; d < D; ++d)
+            dq_row[d] = 0.0;
+        for (int64_t j = 0; j < Lk; ++j) {
+            if (!allowed(i, j, causal))
+                continue;
+            for (int64_t d = 0; d < D; ++d) {
+                dq_row[d] += dp[j] * k[j * D + d];
+                dk[j * D + d] += dp[j] * q_row[d];
+                dv[j * D + d] += p[j] * do_row[d];
+            }
+        }
+        for (int64_t d = 0; d < D; ++d)
+            dq_row[d] *= scale;
+    }
+    for (int64_t t = 0; t < Lk * D; ++t)
+        dk[t] *= scale;
+}
+
+/*
+ * Gradients for fp64 inputs, every head: dq (B, H, Lq, D), dk and dv (B, H, Lk,
+ * D); delta (B, H, Lq) optional.  Returns as fa2_oracle_rows.
+ */
+int fa2_oracle_bwd_f64(const double *q, const double *k, const double *v, const double *dout, int64_t B,
+                       int64_t H, int64_t Lq, int64_t Lk, int64_t D, int causal, double scale, double *dq,
+                       double *dk, double *dv, double *delta, int n_threads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0)
+        return 1;
+    int failed = 0;
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)Lk * sizeof(double));
+        double *p = (double *)malloc((size_t)Lk * sizeof(double));
+        double *dp = (double *)malloc((size_t)Lk * sizeof(double));
+        double *o_row = (double *)malloc((size_t)D * sizeof(double));
+        if (!s || !p || !dp || !o_row) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t bh = 0; bh < B * H; ++bh)
+                one_head_bwd(q + bh * Lq * D, k + bh * Lk * D, v + bh * Lk * D, dout + bh * Lq * D, Lq, Lk, D,
+                             causal, scale, dq + bh * Lq * D, dk + bh * Lk * D, dv + bh * Lk * D,
+                             delta ? delta + bh * Lq : NULL, s, p, dp, o_row);
+        }
+        free(s);
+        free(p);
+        free(dp);
+        free(o_row);
+    }
+    return failed ? 2 : 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int fa2_oracle_max_threads(void)
 {
