@@ -166,6 +166,45 @@ fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
                            int causal, float scale, void *stream);
 
 /*
+ * fa2_bwd_workspace_size -- bytes of device workspace fa2_bwd needs: one fp32
+ * per query row (Delta).  Returns FA2_OK; FA2_ERR_INVALID_ARG for bad sizes;
+ * FA2_ERR_UNSUPPORTED for D other than 64 or 128.
+ */
+fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, size_t *bytes);
+
+/*
+ * fa2_bwd -- the backward pass of the same attention ("Chapter 08: Flash
+ * Attention -- blocked attention", section 6): given dout = dL/dO, writes
+ *
+ *     Delta_i = sum_d dout_id * o_id                 (into the workspace)
+ *     dS      = P * (dout V^T - Delta)               (P recomputed from lse)
+ *     dv = P^T dout,   dk = scale * dS^T q,   dq = scale * dS k
+ *
+ * with the same scores, scale and causal rule as fa2_fwd; o and lse must be
+ * that call's outputs for the same q, k, v.  Three kernels run in order on
+ * `stream`: Delta, dq (query tiles resident), dk and dv (key tiles resident).
+ *
+ *   q, k, v, o   device bf16 inputs (layouts as fa2_fwd); lse fp32 [B, H, Lq].
+ *   dout         device bf16 [B, H, Lq, D].
+ *   dq           device bf16 [B, H, Lq, D] output.
+ *   dk, dv       device bf16 [B, H, Lk, D] outputs (zero rows for keys no
+ *                query sees, e.g. causal keys beyond the last query).
+ *   D            64 or 128 (FA2_ERR_UNSUPPORTED otherwise).
+ *   workspace    device pointer, 16-byte aligned, at least
+ *                fa2_bwd_workspace_size() bytes; overwritten (may be NULL
+ *                when Lq == 0, where dk and dv are simply zeroed).
+ *   (other arguments as for fa2_fwd)
+ *
+ * Errors as fa2_fwd, plus FA2_ERR_INVALID_ARG for a missing or misaligned
+ * dout/dq/dk/dv/workspace or a workspace that is too small.
+ */
+fa2_status fa2_bwd(const void *q, const void *k, const void *v, const void *o,
+                   const float *lse, const void *dout, void *dq, void *dk,
+                   void *dv, int B, int H, int Lq, int Lk, int D, int causal,
+                   float scale, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
  * fa2_fwd_from_host -- the same pass starting from, and ending in, HOST
  * memory: copies q, k, v from the host into the caller's device staging
  * buffers, runs the pass, and copies O and LSE back into the caller's host

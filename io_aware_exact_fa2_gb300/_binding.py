@@ -46,6 +46,10 @@ def load_library() -> ctypes.CDLL:
     lib.fa2_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa2_fwd_noalloc.restype = i
     lib.fa2_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.fa2_bwd_workspace_size.restype = i
+    lib.fa2_bwd_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa2_bwd.restype = i
+    lib.fa2_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa2_get_device_error.restype = i
     lib.fa2_get_device_error.argtypes = [vp, ctypes.POINTER(i)]
     lib.fa2_status_string.restype = ctypes.c_char_p
@@ -151,6 +155,43 @@ def fa2_fwd_noalloc(q, k, v, o, lse, causal: bool, scale: float | None = None, s
                            f"the fixed scratch holds {NOALLOC_SCRATCH_BYTES})")
     if st != 0:
         raise Fa2Error(st, "fa2_fwd_noalloc")
+
+
+def fa2_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None, stream=None,
+            workspace=None) -> None:
+    """Backward pass on CUDA tensors: writes dq, dk, dv (bf16) from the forward's o and lse.
+
+    workspace: a float32/uint8 CUDA tensor of at least fa2_bwd_workspace_size bytes
+    (allocated here when not given).
+    """
+    import torch
+    B, H, Lq, Lk, D = _check_shapes(q, k, v, o, lse)
+    for name, t, shape in (("do", do, (B, H, Lq, D)), ("dq", dq, (B, H, Lq, D)), ("dk", dk, (B, H, Lk, D)),
+                           ("dv", dv, (B, H, Lk, D))):
+        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor of shape {shape}")
+    for t in (q, k, v, o, lse, do, dq, dk, dv):
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+    if scale is None:
+        scale = D ** -0.5
+    n = fa2_bwd_workspace_size(B, H, Lq, Lk, D)
+    if workspace is None:
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    st = _lib.fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq, Lk, D, int(bool(causal)), float(scale),
+                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                      _stream_handle(stream, q.device))
+    if st != 0:
+        raise Fa2Error(st, "fa2_bwd")
+
+
+def fa2_bwd_workspace_size(B: int, H: int, Lq: int, Lk: int, D: int) -> int:
+    n = ctypes.c_size_t(0)
+    st = _lib.fa2_bwd_workspace_size(B, H, Lq, Lk, D, ctypes.byref(n))
+    if st != 0:
+        raise Fa2Error(st, "fa2_bwd_workspace_size")
+    return int(n.value)
 
 
 def fa2_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q_dev, k_dev, v_dev, o_dev, lse_dev,

@@ -24,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libfa2_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["fa2_api.cu", "fa2_noalloc.cu", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu", "fa2_fwd_d256.cu"]
+SOURCES = ["fa2_api.cu", "fa2_noalloc.cu", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu", "fa2_fwd_d256.cu", "fa2_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xptxas", "-v",

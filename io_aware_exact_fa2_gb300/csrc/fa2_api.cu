@@ -305,6 +305,76 @@ FA2_EXPORT fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *
                       stream);
 }
 
+FA2_EXPORT fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, size_t *bytes)
+{
+    if (!bytes)
+        return FA2_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (B <= 0 || H <= 0 || Lq < 0 || Lk <= 0 || D <= 0 || static_cast<long long>(B) * H > INT_MAX)
+        return FA2_ERR_INVALID_ARG;
+    if (D != 64 && D != 128)
+        return FA2_ERR_UNSUPPORTED;
+    *bytes = fa2::align256(static_cast<size_t>(B) * H * Lq * sizeof(float));
+    return FA2_OK;
+}
+
+FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                              const void *dout, void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D,
+                              int causal, float scale, void *workspace, size_t workspace_bytes, void *stream)
+{
+    // the forward's own checks cover q, k, v, o, lse, sizes and scale
+    fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
+    if (st != FA2_OK)
+        return st;
+    if (D != 64 && D != 128)
+        return FA2_ERR_UNSUPPORTED;
+    if (!dout || !dq || !dk || !dv || (!workspace && Lq > 0))
+        return FA2_ERR_INVALID_ARG;
+    if (!fa2::aligned(dout, 16) || !fa2::aligned(dq, 16) || !fa2::aligned(dk, 16) || !fa2::aligned(dv, 16) ||
+        (workspace && !fa2::aligned(workspace, 16)))
+        return FA2_ERR_INVALID_ARG;
+    if (workspace_bytes < static_cast<size_t>(B) * H * Lq * sizeof(float))
+        return FA2_ERR_INVALID_ARG;
+    int dev = 0;
+    if ((st = fa2::select_device_of(q, &dev)) != FA2_OK)
+        return st;
+    if (Lq == 0) {   // no queries: every key's gradients are zero
+        const size_t kv_bytes = static_cast<size_t>(B) * H * Lk * D * 2;
+        if (cudaMemsetAsync(dk, 0, kv_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+            cudaMemsetAsync(dv, 0, kv_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FA2_ERR_CUDA;
+        }
+        return FA2_OK;
+    }
+    fa2::BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.delta = static_cast<float *>(workspace);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.B = B;
+    a.H = H;
+    a.Lq = Lq;
+    a.Lk = Lk;
+    a.D = D;
+    a.causal = causal;
+    a.scale = scale;
+    a.err = fa2::device_error_ptr(dev);
+    a.wait_limit_ns = fa2::wait_limit_ns();
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.encode = fa2::encode_fn();
+    a.device = dev;
+    if (!a.err || !a.encode)
+        return FA2_ERR_CUDA;
+    return fa2::launch_bwd(a);
+}
+
 FA2_EXPORT fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                               int Lq, int Lk, int D, int causal, float scale, void *stream)
 {

@@ -1,0 +1,671 @@
+// fa2_bwd_kernel.cuh -- exact FlashAttention-2 backward pass for sm_103a.
+//
+// The method ("Chapter 08: Flash Attention -- blocked attention", section 6):
+// given dO, the forward's O and per-row LSE, recompute the probabilities P
+// instead of storing them, and
+//   6.2  Delta_i = sum_d dO_id O_id                      (one scalar per query row)
+//   6.3  dS = P * (dP - Delta),  dP = dO V^T             (softmax backward)
+//   6.4  dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K
+// with the two loop structures the section gives: K/V tiles stay on chip while
+// query tiles stream past (dK and dV of those keys need every query's P and
+// dS column), and Q tiles stay on chip while key tiles stream past (dQ of those
+// queries needs every key).  Scores are taken to base 2 (scale * log2 e folded
+// into one FMA, LSE * log2 e per row), so P = 2^(s * c - lse2) exactly as in
+// the forward; in natural-log terms the section's ln 2 factors cancel.
+//
+// GB300 mapping, per kernel:
+//   * TMA (128B swizzle) moves the resident tiles once and the streamed tiles
+//     through a ring; one warp issues tcgen05.mma (elected lane); four warps
+//     (one TMEM lane = one row each) do the elementwise work.
+//   * The two score-like products of a step (S and dP, or their transposes)
+//     go into one of two TMEM buffer pairs, so the next step's pair is computed
+//     while the elementwise warps work on this one.  P and dS are written back
+//     over them as bf16 and read by the gradient MMAs straight from TMEM; the
+//     streamed tiles serve as the MMA's B operand both K-major (for S, dP) and
+//     MN-major (for dV, dK, dQ) without a transpose pass.
+//   * Every wait is bounded (a device error word records which one ran out).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa2 {
+
+struct BwdParams {
+    const float *lse;       // fp32 [B*H, Lq], natural log (the forward's output)
+    const float *delta;     // fp32 [B*H, Lq]
+    uint16_t *dq;           // bf16 [B*H, Lq, D]
+    uint16_t *dk, *dv;      // bf16 [B*H, Lk, D]
+    int *err;
+    unsigned long long wait_limit_ns;
+    int Lq, Lk, BH;
+    int causal;
+    float scale;            // softmax scale (dK, dQ carry it)
+    float scale_log2;       // scale * log2(e)
+};
+
+enum : int {
+    ERR_BWD_PRODUCER = 0x500,
+    ERR_BWD_MMA = 0x600,
+    ERR_BWD_ELEM = 0x700,
+};
+
+constexpr float BWD_LOG2E = 1.4426950408889634074f;
+
+// All lanes wait (bounded) and agree on the outcome, so warp-collective tcgen05
+// instructions that follow run on all lanes or none.
+__device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, int *err, int code,
+                                              unsigned long long limit)
+{
+    const bool ok = ptx::mbar_wait(bar, parity, err, code, limit);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------- Delta (6.2)
+// One warp per query row: Delta = sum_d dO * O in fp32 from the bf16 tensors.
+template <int D>
+__global__ void __launch_bounds__(256) fa2_bwd_delta_kernel(const uint16_t *__restrict__ o,
+                                                            const uint16_t *__restrict__ dout,
+                                                            float *__restrict__ delta, long long rows)
+{
+    const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows)
+        return;
+    constexpr int PER = D / 32;   // elements per lane (2, 4 or 8)
+    const uint16_t *orow = o + r * D + lane * PER;
+    const uint16_t *drow = dout + r * D + lane * PER;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+        const float a = __uint_as_float(static_cast<uint32_t>(orow[e]) << 16);
+        const float b = __uint_as_float(static_cast<uint32_t>(drow[e]) << 16);
+        acc = fmaf(a, b, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0)
+        delta[r] = acc;
+}
+
+// Shared configuration of the two gradient kernels: RES rows of the resident
+// tiles (TMEM lanes), STR rows per streamed tile, head dimension D.
+template <int D_, int RES_, int STR_, int RING_>
+struct BwdCfg {
+    static constexpr int D = D_;
+    static constexpr int RES = RES_;     // resident rows per CTA (= 128 TMEM lanes)
+    static constexpr int STR = STR_;     // rows of a streamed tile per step
+    static constexpr int RING = RING_;   // streamed-tile ring stages
+    static constexpr int DB = D / 64;    // 64-column (128-byte) swizzle blocks
+    static constexpr int RES_BLOCK = RES * 128;
+    static constexpr int RES_TILE = DB * RES_BLOCK;
+    static constexpr int STR_BLOCK = STR * 128;
+    static constexpr int STR_TILE = DB * STR_BLOCK;
+    // shared memory: two resident tiles, the ring (two streamed tiles per stage),
+    // per-stage row statistics (two floats per streamed row), barriers
+    static constexpr int OFF_RES0 = 0;
+    static constexpr int OFF_RES1 = RES_TILE;
+    static constexpr int OFF_STR0 = 2 * RES_TILE;                 // [RING]
+    static constexpr int OFF_STR1 = OFF_STR0 + RING * STR_TILE;    // [RING]
+    static constexpr int OFF_STAT = OFF_STR1 + RING * STR_TILE;    // [RING][2][STR] f32
+    static constexpr int OFF_BAR = OFF_STAT + RING * 2 * STR * 4;
+    static constexpr int BAR_RES_FULL = 0;
+    static constexpr int BAR_STR_FULL = 1;                  // [RING]
+    static constexpr int BAR_STR_EMPTY = BAR_STR_FULL + RING;   // [RING]
+    static constexpr int BAR_PAIR_FULL = BAR_STR_EMPTY + RING;  // [2] score pair computed
+    static constexpr int BAR_PAIR_READY = BAR_PAIR_FULL + 2;    // [2] bf16 operands written
+    static constexpr int BAR_DONE = BAR_PAIR_READY + 2;         // every MMA completed
+    static constexpr int NUM_BARS = BAR_DONE + 1;
+    static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;
+    static constexpr int NUM_THREADS = 192;   // 4 elementwise warps, producer, MMA
+    static constexpr int WARP_PRODUCER = 4;
+    static constexpr int WARP_MMA = 5;
+    static constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(RES, STR, false, false);
+    static constexpr uint32_t IDESC_GRAD = ptx::idesc_bf16_f32(RES, D, false, true);
+    static_assert(D == 64 || D == 128, "gradient kernels support D = 64 and 128");
+    static_assert(RES == 128 && STR % 16 == 0 && STR >= 32 && STR <= 128, "tile shape");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
+};
+
+// bf16 pair from two fp32 values (round to nearest even)
+__device__ __forceinline__ uint32_t bwd_pack(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
+
+// Write this thread's row of a D-column fp32 TMEM accumulator, times `mul`, as bf16
+// to global memory (row `valid` == false: nothing is stored).
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, uint16_t *row_ptr, bool valid)
+{
+    using namespace ptx;
+#pragma unroll 1
+    for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(taddr + 32 * cc, r);
+        tmem_ld_wait(r);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            w[e] = bwd_pack(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+        if (valid) {
+            uint4 *dst = reinterpret_cast<uint4 *>(row_ptr + 32 * cc);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+    }
+}
+
+// ============================================================== dK, dV kernel
+// CTA = one tile of RES = 128 keys of one (b, h); steps = query tiles of STR rows.
+// TMEM: dV (D cols), dK (D cols), two S^T buffers and two dP^T buffers (STR cols
+// each; P^T and dS^T overwrite their first STR/2 columns as bf16 pairs).
+template <class C>
+__global__ void __launch_bounds__(C::NUM_THREADS, 1)
+    fa2_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                      const BwdParams p)
+{
+    using namespace ptx;
+    constexpr int TM_DV = 0, TM_DK = C::D, TM_ST = 2 * C::D, TM_DPT = 2 * C::D + 2 * C::STR;
+    constexpr int TMEM_COLS = 512;
+    static_assert(2 * C::D + 4 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *sgen = smem_raw + (sbase - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+
+    // key tiles in order (heaviest first when causal: low keys are seen by the most queries)
+    const int n_kt = (p.Lk + C::RES - 1) / C::RES;
+    const int kt = static_cast<int>(blockIdx.x) / p.BH;
+    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    if (kt >= n_kt)
+        return;
+    const int k0 = kt * C::RES;
+    const int n_qt = (p.Lq + C::STR - 1) / C::STR;
+    // causal (top-left): query i sees key j iff j <= i, so query tiles before the
+    // one holding row k0 see none of these keys
+    const int qt0 = p.causal ? min(k0 / C::STR, n_qt) : 0;
+    const int n_steps = n_qt - qt0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::BAR_RES_FULL), 1);
+        for (int s = 0; s < C::RING; ++s) {
+            mbar_init(bar(C::BAR_STR_FULL + s), 1);
+            mbar_init(bar(C::BAR_STR_EMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(C::BAR_PAIR_FULL + b), 1);
+            mbar_init(bar(C::BAR_PAIR_READY + b), 4);   // one arrival per elementwise warp
+        }
+        mbar_init(bar(C::BAR_DONE), 1);
+        fence_mbar_init();
+    }
+    if (warp == C::WARP_MMA) {
+        tmem_alloc(sbase + C::OFF_TMEM_SLOT, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEM_SLOT);
+
+    if (warp == C::WARP_PRODUCER) {
+        // ------------------------------------------------ TMA producer (whole warp)
+        bool ok = true;
+        if (n_steps > 0) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_do);
+                mbar_arrive_expect_tx(bar(C::BAR_RES_FULL), 2 * C::RES_TILE);
+#pragma unroll
+                for (int c = 0; c < C::DB; ++c) {
+                    tma_load_3d(sbase + C::OFF_RES0 + c * C::RES_BLOCK, &tm_k, 64 * c, k0, bh, bar(C::BAR_RES_FULL));
+                    tma_load_3d(sbase + C::OFF_RES1 + c * C::RES_BLOCK, &tm_v, 64 * c, k0, bh, bar(C::BAR_RES_FULL));
+                }
+            }
+            const float *lse_h = p.lse + static_cast<size_t>(bh) * p.Lq;
+            const float *delta_h = p.delta + static_cast<size_t>(bh) * p.Lq;
+            for (int s = 0; s < n_steps && ok; ++s) {
+                const int st = s % C::RING;
+                if (s >= C::RING)
+                    ok = mbar_wait(bar(C::BAR_STR_EMPTY + st), ((s / C::RING) - 1) & 1, p.err,
+                                   ERR_BWD_PRODUCER | 1, p.wait_limit_ns);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok)
+                    break;
+                // row statistics of this query tile: lse2 (+inf past Lq, so P = 0 there)
+                // and Delta (0 past Lq)
+                const int q0 = (qt0 + s) * C::STR;
+                float *stat = reinterpret_cast<float *>(sgen + C::OFF_STAT + st * 2 * C::STR * 4);
+                for (int r = lane; r < C::STR; r += 32) {
+                    const int qi = q0 + r;
+                    stat[r] = qi < p.Lq ? lse_h[qi] * BWD_LOG2E : INFINITY;
+                    stat[C::STR + r] = qi < p.Lq ? delta_h[qi] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(C::BAR_STR_FULL + st), 2 * C::STR_TILE);
+#pragma unroll
+                    for (int c = 0; c < C::DB; ++c) {
+                        tma_load_3d(sbase + C::OFF_STR0 + st * C::STR_TILE + c * C::STR_BLOCK, &tm_q, 64 * c, q0,
+                                    bh, bar(C::BAR_STR_FULL + st));
+                        tma_load_3d(sbase + C::OFF_STR1 + st * C::STR_TILE + c * C::STR_BLOCK, &tm_do, 64 * c, q0,
+                                    bh, bar(C::BAR_STR_FULL + st));
+                    }
+                }
+                __syncwarp();
+            }
+            // every load this warp started has landed before the CTA may exit
+            if (lane == 0) {
+                mbar_wait(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_PRODUCER | 2, p.wait_limit_ns);
+                const int issued = ok ? n_steps : 0;
+                for (int s = issued > C::RING ? issued - C::RING : 0; s < issued; ++s)
+                    mbar_wait(bar(C::BAR_STR_FULL + s % C::RING), (s / C::RING) & 1, p.err, ERR_BWD_PRODUCER | 3,
+                              p.wait_limit_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == C::WARP_MMA) {
+        // ------------------------------------------------ MMA issuer (elected lane)
+        const bool leader = elect_one();
+        bool ok = true;
+        if (n_steps > 0) {
+            const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
+            const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
+            const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
+            const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
+            // the same streamed tiles as MN-major B operands (N = D along the rows'
+            // 128-byte lines, K = query rows)
+            const uint64_t desc_q_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
+            const uint64_t desc_do_mn = sdesc_sw128(sbase + C::OFF_STR1, C::STR_BLOCK, 1024);
+            ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
+            tc_fence_after();
+            // S^T(b) = K Q^T and dP^T(b) = V dO^T for step s
+            auto issue_pair = [&](int s) -> bool {
+                const int st = s % C::RING, b = s & 1;
+                if (!warp_wait_all(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_MMA | 2,
+                                   p.wait_limit_ns))
+                    return false;
+                tc_fence_after();
+                if (leader) {
+                    const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < C::D / 16; ++kk) {
+                        const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4);
+                        const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
+                        mma_ss(tmem + TM_ST + b * C::STR, desc_k + ro, desc_q + so + to, C::IDESC_PAIR,
+                               kk > 0 ? 1u : 0u);
+                        mma_ss(tmem + TM_DPT + b * C::STR, desc_v + ro, desc_do + so + to, C::IDESC_PAIR,
+                               kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar(C::BAR_PAIR_FULL + b));
+                }
+                __syncwarp();
+                return true;
+            };
+            // dV += P^T dO and dK += dS^T Q for step s
+            auto issue_grad = [&](int s) -> bool {
+                const int st = s % C::RING, b = s & 1;
+                if (!warp_wait_all(bar(C::BAR_PAIR_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 3,
+                                   p.wait_limit_ns))
+                    return false;
+                tc_fence_after();
+                if (leader) {
+                    const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < C::STR / 16; ++kk) {
+                        const uint64_t ko = static_cast<uint64_t>((kk * 16 * 128) >> 4);   // 16 rows
+                        const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+                        mma_ts(tmem + TM_DV, tmem + TM_ST + b * C::STR + kk * 8, desc_do_mn + so + ko,
+                               C::IDESC_GRAD, acc);
+                        mma_ts(tmem + TM_DK, tmem + TM_DPT + b * C::STR + kk * 8, desc_q_mn + so + ko,
+                               C::IDESC_GRAD, acc);
+                    }
+                    mma_commit(bar(C::BAR_STR_EMPTY + st));   // this step's Q, dO and stats are free
+                }
+                __syncwarp();
+                return true;
+            };
+            if (ok)
+                ok = issue_pair(0);
+            if (ok && n_steps > 1)
+                ok = issue_pair(1);
+            for (int s = 0; s < n_steps && ok; ++s) {
+                ok = issue_grad(s);
+                if (ok && s + 2 < n_steps)
+                    ok = issue_pair(s + 2);   // into the buffers issue_grad(s) just read
+            }
+            if (leader)
+                mma_commit(bar(C::BAR_DONE));
+            __syncwarp();
+            warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 4, p.wait_limit_ns);
+        }
+    } else {
+        // ------------------------------------------------ elementwise warps
+        const int row = warp * 32 + lane;            // key row within the tile (TMEM lane)
+        const int kj = k0 + row;                     // key index
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const float c2 = p.scale_log2;
+        bool ok = true;
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const int st = s % C::RING, b = s & 1;
+            ok = warp_wait_all(bar(C::BAR_PAIR_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 1, p.wait_limit_ns);
+            if (!ok)
+                break;
+            tc_fence_after();
+            // the row statistics were written by the producer warp before it armed
+            // this stage's barrier: acquire them from that barrier directly (it cannot
+            // have moved on, since the stage is only refilled after this step's MMAs)
+            ok = warp_wait_all(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_ELEM | 5,
+                               p.wait_limit_ns);
+            if (!ok)
+                break;
+            const uint32_t a_st = tmem + lane_base + TM_ST + b * C::STR;
+            const uint32_t a_dp = tmem + lane_base + TM_DPT + b * C::STR;
+            const float *stat = reinterpret_cast<const float *>(sgen + C::OFF_STAT + st * 2 * C::STR * 4);
+            const int q0 = (qt0 + s) * C::STR;
+            // query columns c with q0 + c < kj are masked (causal, key after query)
+            const int first_visible = p.causal ? kj - q0 : 0;
+            uint32_t pw[C::STR / 2], dw[C::STR / 2];
+#pragma unroll
+            for (int ch = 0; ch < C::STR / 32; ++ch) {
+                uint32_t rs[32], rd[32];
+                tmem_ld32(a_st + 32 * ch, rs);
+                tmem_ld32(a_dp + 32 * ch, rd);
+                tmem_ld_wait(rs);
+                tmem_ld_wait(rd);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int c = 32 * ch + e;
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float lse2 = stat[c + u];
+                        const float dl = stat[C::STR + c + u];
+                        float pp = ex2_approx(fmaf(__uint_as_float(rs[e + u]), c2, -lse2));
+                        if (c + u < first_visible)
+                            pp = 0.f;
+                        pv[u] = pp;
+                        dv[u] = pp * (__uint_as_float(rd[e + u]) - dl);
+                    }
+                    pw[c / 2] = bwd_pack(pv[0], pv[1]);
+                    dw[c / 2] = bwd_pack(dv[0], dv[1]);
+                }
+            }
+            // P^T and dS^T as bf16 pairs over the first STR/2 columns of their buffers
+            if constexpr (C::STR / 2 >= 32) {
+#pragma unroll
+                for (int q = 0; q < C::STR / 64; ++q) {
+                    tmem_st32(a_st + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32 * q));
+                    tmem_st32(a_dp + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(dw + 32 * q));
+                }
+            } else {
+                tmem_st16(a_st, pw);
+                tmem_st16(a_dp, dw);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(C::BAR_PAIR_READY + b));
+        }
+        // epilogue: dV and scale * dK rows (zeros when no query sees these keys)
+        const bool valid = kj < p.Lk;
+        uint16_t *dv_row = p.dv + (static_cast<size_t>(bh) * p.Lk + (valid ? kj : 0)) * C::D;
+        uint16_t *dk_row = p.dk + (static_cast<size_t>(bh) * p.Lk + (valid ? kj : 0)) * C::D;
+        if (n_steps == 0) {
+            if (valid) {
+                for (int d = 0; d < C::D; d += 8) {
+                    *reinterpret_cast<uint4 *>(dv_row + d) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(dk_row + d) = make_uint4(0, 0, 0, 0);
+                }
+            }
+        } else if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 2, p.wait_limit_ns)) {
+            tc_fence_after();
+            store_acc_row<C::D>(tmem + lane_base + TM_DV, 1.f, dv_row, valid);
+            store_acc_row<C::D>(tmem + lane_base + TM_DK, p.scale, dk_row, valid);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ================================================================= dQ kernel
+// CTA = one tile of RES = 128 queries of one (b, h); steps = key tiles of STR rows.
+// TMEM: dQ (D cols), two S buffers and two dP buffers (STR cols each; dS
+// overwrites the first STR/2 columns of its S buffer as bf16 pairs).
+template <class C>
+__global__ void __launch_bounds__(C::NUM_THREADS, 1)
+    fa2_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const BwdParams p)
+{
+    using namespace ptx;
+    constexpr int TM_DQ = 0, TM_S = C::D, TM_DP = C::D + 2 * C::STR;
+    constexpr int TMEM_COLS = 512;
+    static_assert(C::D + 4 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *sgen = smem_raw + (sbase - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+
+    // query tiles, last (heaviest when causal) first
+    const int n_qt = (p.Lq + C::RES - 1) / C::RES;
+    const int qt = n_qt - 1 - static_cast<int>(blockIdx.x) / p.BH;
+    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    if (qt < 0)
+        return;
+    const int q0 = qt * C::RES;
+    // key tiles this query tile visits (causal: up to its last row's key)
+    const int n_kt_all = (p.Lk + C::STR - 1) / C::STR;
+    const int last_row = min(q0 + C::RES - 1, p.Lq - 1);
+    const int n_steps = p.causal ? min(min(last_row, p.Lk - 1) / C::STR + 1, n_kt_all) : n_kt_all;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::BAR_RES_FULL), 1);
+        for (int s = 0; s < C::RING; ++s) {
+            mbar_init(bar(C::BAR_STR_FULL + s), 1);
+            mbar_init(bar(C::BAR_STR_EMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(C::BAR_PAIR_FULL + b), 1);
+            mbar_init(bar(C::BAR_PAIR_READY + b), 4);
+        }
+        mbar_init(bar(C::BAR_DONE), 1);
+        fence_mbar_init();
+    }
+    if (warp == C::WARP_MMA) {
+        tmem_alloc(sbase + C::OFF_TMEM_SLOT, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + C::OFF_TMEM_SLOT);
+
+    if (warp == C::WARP_PRODUCER) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_do);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(bar(C::BAR_RES_FULL), 2 * C::RES_TILE);
+#pragma unroll
+            for (int c = 0; c < C::DB; ++c) {
+                tma_load_3d(sbase + C::OFF_RES0 + c * C::RES_BLOCK, &tm_q, 64 * c, q0, bh, bar(C::BAR_RES_FULL));
+                tma_load_3d(sbase + C::OFF_RES1 + c * C::RES_BLOCK, &tm_do, 64 * c, q0, bh, bar(C::BAR_RES_FULL));
+            }
+            bool ok = true;
+            int issued = 0;
+            for (int s = 0; s < n_steps && ok; ++s) {
+                const int st = s % C::RING;
+                if (s >= C::RING &&
+                    !mbar_wait(bar(C::BAR_STR_EMPTY + st), ((s / C::RING) - 1) & 1, p.err, ERR_BWD_PRODUCER | 4,
+                               p.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int j0 = s * C::STR;
+                mbar_arrive_expect_tx(bar(C::BAR_STR_FULL + st), 2 * C::STR_TILE);
+#pragma unroll
+                for (int c = 0; c < C::DB; ++c) {
+                    tma_load_3d(sbase + C::OFF_STR0 + st * C::STR_TILE + c * C::STR_BLOCK, &tm_k, 64 * c, j0, bh,
+                                bar(C::BAR_STR_FULL + st));
+                    tma_load_3d(sbase + C::OFF_STR1 + st * C::STR_TILE + c * C::STR_BLOCK, &tm_v, 64 * c, j0, bh,
+                                bar(C::BAR_STR_FULL + st));
+                }
+                ++issued;
+            }
+            mbar_wait(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_PRODUCER | 5, p.wait_limit_ns);
+            for (int s = issued > C::RING ? issued - C::RING : 0; s < issued; ++s)
+                mbar_wait(bar(C::BAR_STR_FULL + s % C::RING), (s / C::RING) & 1, p.err, ERR_BWD_PRODUCER | 6,
+                          p.wait_limit_ns);
+        }
+        __syncwarp();
+    } else if (warp == C::WARP_MMA) {
+        const bool leader = elect_one();
+        const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
+        const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
+        const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
+        const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
+        const uint64_t desc_k_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
+        bool ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
+        tc_fence_after();
+        // S(b) = Q K^T and dP(b) = dO V^T for step s
+        auto issue_pair = [&](int s) -> bool {
+            const int st = s % C::RING, b = s & 1;
+            if (!warp_wait_all(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_MMA | 6,
+                               p.wait_limit_ns))
+                return false;
+            tc_fence_after();
+            if (leader) {
+                const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < C::D / 16; ++kk) {
+                    const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4);
+                    const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + TM_S + b * C::STR, desc_q + ro, desc_k + so + to, C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + TM_DP + b * C::STR, desc_do + ro, desc_v + so + to, C::IDESC_PAIR,
+                           kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(C::BAR_PAIR_FULL + b));
+            }
+            __syncwarp();
+            return true;
+        };
+        // dQ += dS K for step s
+        auto issue_grad = [&](int s) -> bool {
+            const int st = s % C::RING, b = s & 1;
+            if (!warp_wait_all(bar(C::BAR_PAIR_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 7, p.wait_limit_ns))
+                return false;
+            tc_fence_after();
+            if (leader) {
+                const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < C::STR / 16; ++kk)
+                    mma_ts(tmem + TM_DQ, tmem + TM_S + b * C::STR + kk * 8,
+                           desc_k_mn + so + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_GRAD,
+                           (s > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(C::BAR_STR_EMPTY + st));
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok)
+            ok = issue_pair(0);
+        if (ok && n_steps > 1)
+            ok = issue_pair(1);
+        for (int s = 0; s < n_steps && ok; ++s) {
+            ok = issue_grad(s);
+            if (ok && s + 2 < n_steps)
+                ok = issue_pair(s + 2);
+        }
+        if (leader)
+            mma_commit(bar(C::BAR_DONE));
+        __syncwarp();
+        warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 8, p.wait_limit_ns);
+    } else {
+        const int row = warp * 32 + lane;            // query row within the tile
+        const int qi = q0 + row;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const float c2 = p.scale_log2;
+        const bool live = qi < p.Lq;
+        const size_t srow = static_cast<size_t>(bh) * p.Lq + (live ? qi : 0);
+        const float lse2 = live ? p.lse[srow] * BWD_LOG2E : INFINITY;
+        const float dl = live ? p.delta[srow] : 0.f;
+        // keys j < lim are visible to this row
+        const int lim = p.causal ? min(qi + 1, p.Lk) : p.Lk;
+        bool ok = true;
+        for (int s = 0; s < n_steps && ok; ++s) {
+            const int b = s & 1;
+            ok = warp_wait_all(bar(C::BAR_PAIR_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 3, p.wait_limit_ns);
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t a_s = tmem + lane_base + TM_S + b * C::STR;
+            const uint32_t a_dp = tmem + lane_base + TM_DP + b * C::STR;
+            const int j0 = s * C::STR;
+            const bool masked = j0 + C::STR > lim;
+            uint32_t dw[C::STR / 2];
+#pragma unroll
+            for (int ch = 0; ch < C::STR / 32; ++ch) {
+                uint32_t rs[32], rd[32];
+                tmem_ld32(a_s + 32 * ch, rs);
+                tmem_ld32(a_dp + 32 * ch, rd);
+                tmem_ld_wait(rs);
+                tmem_ld_wait(rd);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float dv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        float pp = ex2_approx(fmaf(__uint_as_float(rs[e + u]), c2, -lse2));
+                        if (masked && j0 + 32 * ch + e + u >= lim)
+                            pp = 0.f;
+                        dv[u] = pp * (__uint_as_float(rd[e + u]) - dl);
+                    }
+                    dw[(32 * ch + e) / 2] = bwd_pack(dv[0], dv[1]);
+                }
+            }
+            if constexpr (C::STR / 2 >= 32) {
+#pragma unroll
+                for (int q = 0; q < C::STR / 64; ++q)
+                    tmem_st32(a_s + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(dw + 32 * q));
+            } else {
+                tmem_st16(a_s, dw);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(C::BAR_PAIR_READY + b));
+        }
+        if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 4, p.wait_limit_ns)) {
+            tc_fence_after();
+            store_acc_row<C::D>(tmem + lane_base + TM_DQ, p.scale, p.dq + srow * C::D, live);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace fa2

@@ -156,6 +156,23 @@ fa2_status launch_fwd(const LaunchArgs &a)
     return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
+// Arguments of the backward pass (fa2_bwd.cu).
+struct BwdArgs {
+    const void *q, *k, *v, *o, *dout;
+    const float *lse;
+    float *delta;             // workspace: B*H*Lq fp32
+    void *dq, *dk, *dv;
+    int B, H, Lq, Lk, D;
+    int causal;
+    float scale;
+    int *err;
+    unsigned long long wait_limit_ns;
+    cudaStream_t stream;
+    EncodeTiledFn encode;
+    int device;
+};
+fa2_status launch_bwd(const BwdArgs &a);
+
 // One entry per head dimension (defined in fa2_fwd_d{64,128,256}.cu).
 fa2_status launch_fwd_d64(const LaunchArgs &a);
 fa2_status launch_fwd_d128(const LaunchArgs &a);

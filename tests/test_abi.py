@@ -32,9 +32,9 @@ def header_functions():
 
 
 def test_header_declares_the_boundary():
-    assert header_functions() == ["fa2_fwd", "fa2_fwd_from_host", "fa2_fwd_noalloc", "fa2_fwd_ws",
-                                  "fa2_get_device_error", "fa2_status_string", "fa2_version",
-                                  "fa2_workspace_size"]
+    assert header_functions() == ["fa2_bwd", "fa2_bwd_workspace_size", "fa2_fwd", "fa2_fwd_from_host",
+                                  "fa2_fwd_noalloc", "fa2_fwd_ws", "fa2_get_device_error", "fa2_status_string",
+                                  "fa2_version", "fa2_workspace_size"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -139,3 +139,27 @@ def test_binding_shape_checks():
     with pytest.raises(ValueError):
         _binding._check_shapes(q, k, k, o, lse[:, :, :7])
     assert _binding._check_shapes(q, k, k, o, lse) == (1, 2, 8, 9, 64)
+
+
+def test_bwd_validation(lib):
+    """Backward entry points reject bad arguments on the host, before any CUDA call."""
+    n = ctypes.c_size_t(0)
+    assert lib.fa2_bwd_workspace_size(2, 3, 100, 50, 128, ctypes.byref(n)) == OK
+    assert n.value >= 2 * 3 * 100 * 4 and n.value % 256 == 0
+    assert lib.fa2_bwd_workspace_size(2, 3, 100, 50, 256, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.fa2_bwd_workspace_size(0, 3, 100, 50, 64, ctypes.byref(n)) == INVALID
+    f = lib.fa2_bwd
+    good = dict(q=P, k=P, v=P, o=P, lse=P, do=P, dq=P, dk=P, dv=P, B=1, H=1, Lq=8, Lk=8, D=64, causal=0,
+                scale=0.125, ws=P, ws_bytes=4096)
+
+    def call_bwd(**kw):
+        a = dict(good, **kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["B"], a["H"],
+                 a["Lq"], a["Lk"], a["D"], a["causal"], a["scale"], a["ws"], a["ws_bytes"], None)
+    assert call_bwd(do=0) == INVALID
+    assert call_bwd(dq=P + 8) == INVALID
+    assert call_bwd(dk=0) == INVALID
+    assert call_bwd(ws=0) == INVALID
+    assert call_bwd(ws_bytes=4) == INVALID
+    assert call_bwd(D=256) == UNSUPPORTED
+    assert call_bwd(scale=float("nan")) == INVALID
