@@ -306,6 +306,34 @@ def run_ours(args, world, rank, local):
     in_bytes = (q.numel() + k.numel() + v.numel()) * 2
     out_bytes = o.numel() * 2 + lse.numel() * 4
 
+    # ---- backward pass (context, not the headline metric): its own timed region
+    backward = None
+    if not args.no_backward and w.D in (64, 128):
+        from io_aware_exact_fa2_gb300 import fa2_bwd, fa2_bwd_workspace_size
+        g = torch.Generator(device="cpu").manual_seed(w.seed_base + 7)
+        dout = torch.randn(w.B, w.H, w.Lq, w.D, generator=g).to(torch.bfloat16).to(dev)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        bws = torch.empty(max(fa2_bwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D), 16), dtype=torch.uint8, device=dev)
+        bwd_ms = []
+        for causal in modes:
+            fa2_fwd(qd, kd, vd, o, lse, causal, w.scale, stream=stream)
+            for _ in range(max(2, args.warmup)):
+                fa2_bwd(qd, kd, vd, o, lse, dout, dq, dk, dv, causal, w.scale, stream=stream, workspace=bws)
+            evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            barrier(world)
+            for s_ in range(args.steps):
+                flush.fill_(float(s_))
+                evb[s_][0].record(stream)
+                fa2_bwd(qd, kd, vd, o, lse, dout, dq, dk, dv, causal, w.scale, stream=stream, workspace=bws)
+                evb[s_][1].record(stream)
+            torch.cuda.synchronize(dev)
+            bwd_ms.append(max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evb])), world, dev))
+        st, code = fa2_get_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error {st} code {code:#x} in the backward pass")
+        backward = (bwd_ms, )
+
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
@@ -346,6 +374,19 @@ def run_ours(args, world, rank, local):
     if cpu_val is not None:
         line["cpu_baseline"] = {"value": cpu_val, "unit": UNIT, "cores": cpu_threads, "kind": "oracle",
                                 "sample": cpu_desc}
+    if backward is not None:
+        bwd = {}
+        for i, c in enumerate(modes):
+            ms = backward[0][i]
+            tf = 2.5 * w.flops(c) / (ms * 1e-3) / 1e12
+            bwd["causal" if c else "noncausal"] = {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak}
+        line["backward"] = {
+            "metric": "attention bwd TFLOP/s (FLOPs = 2.5 x the forward's: the five matmuls of dS, dP, dV, "
+                      "dK, dQ; the kernels also recompute S and dP for dQ)",
+            "unit": UNIT, "per_mode": bwd,
+            "kernels": "Delta, dQ (query tiles resident), dK/dV (key tiles resident) per call (fa2_bwd)",
+            "l2": "flushed (256 MiB write) before every timed call"}
+    print(json.dumps(line), flush=True)
     print(json.dumps(line), flush=True)
 
 
@@ -359,6 +400,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
