@@ -8,11 +8,12 @@
 
 namespace fa2 {
 
-// dK/dV: 128 keys resident, query tiles of 64 streamed through a 3-stage ring;
-// dQ: 128 queries resident, key tiles of 64.  Two 64-column score buffer pairs
-// let one step's MMAs run while the previous step's elementwise work finishes.
+// dK/dV: 128 keys resident, query tiles of 32 streamed through a 4-stage ring
+// (dV, dK, two 32-column score pairs and K, V as MMA operands fill TMEM);
+// dQ: 128 queries resident, key tiles of 64.  Two score buffer pairs let one
+// step's MMAs run while the previous step's elementwise work finishes.
 template <int D>
-using BwdKV = BwdCfg<D, 128, 64, 3>;
+using BwdKV = BwdCfg<D, 128, 32, 4>;
 template <int D>
 using BwdQ = BwdCfg<D, 128, 64, 3>;
 

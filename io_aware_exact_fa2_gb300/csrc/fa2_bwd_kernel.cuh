@@ -118,7 +118,8 @@ struct BwdCfg {
     static constexpr int BAR_PAIR_FULL = BAR_STR_EMPTY + RING;  // [2] score pair computed
     static constexpr int BAR_PAIR_READY = BAR_PAIR_FULL + 2;    // [2] bf16 operands written
     static constexpr int BAR_DONE = BAR_PAIR_READY + 2;         // every MMA completed
-    static constexpr int NUM_BARS = BAR_DONE + 1;
+    static constexpr int BAR_RES_TMEM = BAR_DONE + 1;           // resident tiles copied into TMEM
+    static constexpr int NUM_BARS = BAR_RES_TMEM + 1;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;
     static constexpr int NUM_THREADS = 192;   // 4 elementwise warps, producer, MMA
@@ -130,6 +131,24 @@ struct BwdCfg {
     static_assert(RES == 128 && STR % 16 == 0 && STR >= 32 && STR <= 128, "tile shape");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
+
+// This thread's row of a resident tile (RES rows, 128B-swizzled 64-column blocks:
+// 16-byte piece c of row r sits at c ^ (r % 8)) into TMEM as packed bf16 pairs,
+// two per column -- the layout of an MMA A operand read from TMEM.
+template <int DB, int BLOCK>
+__device__ __forceinline__ void copy_row_to_tmem(uint32_t smem_tile, int row, uint32_t tmem_dst)
+{
+    using namespace ptx;
+#pragma unroll
+    for (int bq = 0; bq < DB; ++bq) {
+        const uint32_t src = smem_tile + bq * BLOCK + row * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            ld_shared_v4(src + ((c ^ (row & 7)) * 16), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        tmem_st32(tmem_dst + bq * 32, w);
+    }
+}
 
 // bf16 pair from two fp32 values (round to nearest even)
 __device__ __forceinline__ uint32_t bwd_pack(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
@@ -169,9 +188,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                       const BwdParams p)
 {
     using namespace ptx;
+    // K and V are also copied into TMEM (TM_KA, TM_VA) so that S^T = K Q^T and
+    // dP^T = V dO^T read their A operand from TMEM instead of loading it from
+    // shared memory for every instruction
     constexpr int TM_DV = 0, TM_DK = C::D, TM_ST = 2 * C::D, TM_DPT = 2 * C::D + 2 * C::STR;
+    constexpr int TM_KA = 2 * C::D + 4 * C::STR, TM_VA = TM_KA + C::D / 2;
     constexpr int TMEM_COLS = 512;
-    static_assert(2 * C::D + 4 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
+    static_assert(TM_VA + C::D / 2 <= TMEM_COLS, "TMEM budget exceeded");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -203,6 +226,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_init(bar(C::BAR_PAIR_READY + b), 4);   // one arrival per elementwise warp
         }
         mbar_init(bar(C::BAR_DONE), 1);
+        mbar_init(bar(C::BAR_RES_TMEM), 4);   // one arrival per elementwise warp
         fence_mbar_init();
     }
     if (warp == C::WARP_MMA) {
@@ -277,15 +301,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const bool leader = elect_one();
         bool ok = true;
         if (n_steps > 0) {
-            const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
-            const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
             const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
             const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
             // the same streamed tiles as MN-major B operands (N = D along the rows'
             // 128-byte lines, K = query rows)
             const uint64_t desc_q_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
             const uint64_t desc_do_mn = sdesc_sw128(sbase + C::OFF_STR1, C::STR_BLOCK, 1024);
-            ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
+            // K and V copied into TMEM by the elementwise warps
+            ok = warp_wait_all(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
             tc_fence_after();
             // S^T(b) = K Q^T and dP^T(b) = V dO^T for step s
             auto issue_pair = [&](int s) -> bool {
@@ -298,11 +321,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < C::D / 16; ++kk) {
-                        const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4);
                         const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                        mma_ss(tmem + TM_ST + b * C::STR, desc_k + ro, desc_q + so + to, C::IDESC_PAIR,
+                        mma_ts(tmem + TM_ST + b * C::STR, tmem + TM_KA + kk * 8, desc_q + so + to, C::IDESC_PAIR,
                                kk > 0 ? 1u : 0u);
-                        mma_ss(tmem + TM_DPT + b * C::STR, desc_v + ro, desc_do + so + to, C::IDESC_PAIR,
+                        mma_ts(tmem + TM_DPT + b * C::STR, tmem + TM_VA + kk * 8, desc_do + so + to, C::IDESC_PAIR,
                                kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(C::BAR_PAIR_FULL + b));
@@ -354,6 +376,19 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         const float c2 = p.scale_log2;
         bool ok = true;
+        if (n_steps > 0) {
+            // this row of K and of V into TMEM, as the score MMAs' A operands
+            ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
+            if (ok) {
+                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_KA);
+                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES1, row, tmem + lane_base + TM_VA);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(C::BAR_RES_TMEM));
+            }
+        }
         for (int s = 0; s < n_steps && ok; ++s) {
             const int st = s % C::RING, b = s & 1;
             ok = warp_wait_all(bar(C::BAR_PAIR_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 1, p.wait_limit_ns);
@@ -453,9 +488,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                      const BwdParams p)
 {
     using namespace ptx;
+    // Q and dO are also copied into TMEM (TM_QA, TM_DOA) so that S = Q K^T and
+    // dP = dO V^T read their A operand from TMEM instead of loading it from shared
+    // memory for every instruction
     constexpr int TM_DQ = 0, TM_S = C::D, TM_DP = C::D + 2 * C::STR;
+    constexpr int TM_QA = C::D + 4 * C::STR, TM_DOA = TM_QA + C::D / 2;
     constexpr int TMEM_COLS = 512;
-    static_assert(C::D + 4 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
+    static_assert(TM_DOA + C::D / 2 <= TMEM_COLS, "TMEM budget exceeded");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -486,6 +525,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_init(bar(C::BAR_PAIR_READY + b), 4);
         }
         mbar_init(bar(C::BAR_DONE), 1);
+        mbar_init(bar(C::BAR_RES_TMEM), 4);   // one arrival per elementwise warp
         fence_mbar_init();
     }
     if (warp == C::WARP_MMA) {
@@ -538,12 +578,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         __syncwarp();
     } else if (warp == C::WARP_MMA) {
         const bool leader = elect_one();
-        const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
-        const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
         const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
         const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
         const uint64_t desc_k_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
-        bool ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
+        // Q and dO copied into TMEM by the elementwise warps
+        bool ok = warp_wait_all(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
         tc_fence_after();
         // S(b) = Q K^T and dP(b) = dO V^T for step s
         auto issue_pair = [&](int s) -> bool {
@@ -556,10 +595,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::D / 16; ++kk) {
-                    const uint64_t ro = static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4);
                     const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + TM_S + b * C::STR, desc_q + ro, desc_k + so + to, C::IDESC_PAIR, kk > 0 ? 1u : 0u);
-                    mma_ss(tmem + TM_DP + b * C::STR, desc_do + ro, desc_v + so + to, C::IDESC_PAIR,
+                    mma_ts(tmem + TM_S + b * C::STR, tmem + TM_QA + kk * 8, desc_k + so + to, C::IDESC_PAIR,
+                           kk > 0 ? 1u : 0u);
+                    mma_ts(tmem + TM_DP + b * C::STR, tmem + TM_DOA + kk * 8, desc_v + so + to, C::IDESC_PAIR,
                            kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::BAR_PAIR_FULL + b));
@@ -609,7 +648,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const float dl = live ? p.delta[srow] : 0.f;
         // keys j < lim are visible to this row
         const int lim = p.causal ? min(qi + 1, p.Lk) : p.Lk;
-        bool ok = true;
+        // this row of Q and of dO into TMEM, as the score MMAs' A operands
+        bool ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
+        if (ok) {
+            copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_QA);
+            copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES1, row, tmem + lane_base + TM_DOA);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(C::BAR_RES_TMEM));
+        }
         for (int s = 0; s < n_steps && ok; ++s) {
             const int b = s & 1;
             ok = warp_wait_all(bar(C::BAR_PAIR_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 3, p.wait_limit_ns);
