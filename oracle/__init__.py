@@ -68,6 +68,13 @@ def _load():
                 ctypes.c_int64, ctypes.c_int, ctypes.c_double,
                 ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.fa2_oracle_rows_w.restype = ctypes.c_int
+            lib.fa2_oracle_rows_w.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
+                ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.fa2_oracle_decode_bf16.restype = None
             lib.fa2_oracle_decode_bf16.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
@@ -75,10 +82,10 @@ def _load():
             lib.fa2_oracle_max_threads.argtypes = []
             i64, vp = ctypes.c_int64, ctypes.c_void_p
             lib.fa2_oracle_fwd_f64.restype = ctypes.c_int
-            lib.fa2_oracle_fwd_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int,
+            lib.fa2_oracle_fwd_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, i64,
                                                ctypes.c_double, vp, vp, ctypes.c_int]
             lib.fa2_oracle_bwd_f64.restype = ctypes.c_int
-            lib.fa2_oracle_bwd_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int,
+            lib.fa2_oracle_bwd_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, i64,
                                                ctypes.c_double, vp, vp, vp, vp, ctypes.c_int]
             _lib = lib
     return _lib
@@ -105,12 +112,23 @@ def max_threads() -> int:
     return int(_load().fa2_oracle_max_threads())
 
 
+def _window_arg(causal: bool, window, Lq: int, Lk: int) -> int:
+    """Sliding window (w, 0) of "Flash Attention: principles and implementation",
+    section 6.3: needs causal, w >= 0, and Lq <= Lk so every row keeps key i."""
+    if window is None:
+        return -1
+    if not causal or window < 0 or Lq > Lk:
+        raise ValueError("a sliding window needs causal=True, window >= 0 and Lq <= Lk")
+    return int(window)
+
+
 def attention_rows(q, k, v, causal: bool, scale: float, rows=None,
-                   return_p: bool = False, threads: int = 0):
+                   return_p: bool = False, threads: int = 0, window=None):
     """Oracle output for selected rows.
 
     q: bf16 (B, H, Lq, D); k, v: bf16 (B, H, Lk, D) (torch CPU or CUDA tensors).
     rows: int64 array of flat row ids (b*H + h)*Lq + i; None means every row.
+    window: None, or w for the causal sliding window i - w <= j <= i.
     Returns (o (n, D) fp64, lse (n,) fp64[, p (n, Lk) fp64]).
     """
     B, H, Lq, D = q.shape
@@ -125,9 +143,10 @@ def attention_rows(q, k, v, causal: bool, scale: float, rows=None,
     o = np.empty((n, D), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
     p = np.empty((n, Lk), dtype=np.float64) if return_p else None
-    rc = _load().fa2_oracle_rows(
+    w = _window_arg(causal, window, Lq, Lk)
+    rc = _load().fa2_oracle_rows_w(
         qb.ctypes.data, kb.ctypes.data, vb.ctypes.data,
-        B, H, Lq, Lk, D, int(bool(causal)), float(scale),
+        B, H, Lq, Lk, D, int(bool(causal)), w, float(scale),
         rows.ctypes.data if n else None, n,
         o.ctypes.data, lse.ctypes.data, p.ctypes.data if return_p else None,
         int(threads))
@@ -136,10 +155,10 @@ def attention_rows(q, k, v, causal: bool, scale: float, rows=None,
     return (o, lse, p) if return_p else (o, lse)
 
 
-def attention(q, k, v, causal: bool, scale: float, threads: int = 0):
+def attention(q, k, v, causal: bool, scale: float, threads: int = 0, window=None):
     """Full oracle output: O fp64 (B, H, Lq, D) and LSE fp64 (B, H, Lq)."""
     B, H, Lq, D = q.shape
-    o, lse = attention_rows(q, k, v, causal, scale, None, False, threads)
+    o, lse = attention_rows(q, k, v, causal, scale, None, False, threads, window)
     return o.reshape(B, H, Lq, D), lse.reshape(B, H, Lq)
 
 
@@ -147,7 +166,7 @@ def _f64(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float64)
 
 
-def forward_f64(q, k, v, causal: bool, scale: float, threads: int = 0):
+def forward_f64(q, k, v, causal: bool, scale: float, threads: int = 0, window=None):
     """Forward definition on fp64 arrays (B, H, L, D): (O fp64 (B, H, Lq, D), LSE (B, H, Lq)).
 
     The same per-row arithmetic as ``attention`` without the bf16 widening, so a
@@ -159,13 +178,14 @@ def forward_f64(q, k, v, causal: bool, scale: float, threads: int = 0):
     o = np.empty((B, H, Lq, D))
     lse = np.empty((B, H, Lq))
     rc = _load().fa2_oracle_fwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Lq, Lk, D,
-                                     int(bool(causal)), float(scale), o.ctypes.data, lse.ctypes.data, int(threads))
+                                     int(bool(causal)), _window_arg(causal, window, Lq, Lk), float(scale),
+                                     o.ctypes.data, lse.ctypes.data, int(threads))
     if rc != 0:
         raise RuntimeError(f"fa2_oracle_fwd_f64 failed with code {rc}")
     return o, lse
 
 
-def gradients_f64(q, k, v, do, causal: bool, scale: float, threads: int = 0):
+def gradients_f64(q, k, v, do, causal: bool, scale: float, threads: int = 0, window=None):
     """Backward definition on fp64 arrays: (dQ, dK, dV, Delta) for L with dL/dO = do.
 
     Chapter 08, section 6: Delta = rowsum(dO * O), dS = P * (dO V^T - Delta),
@@ -179,14 +199,15 @@ def gradients_f64(q, k, v, do, causal: bool, scale: float, threads: int = 0):
     dv = np.empty((B, H, Lk, D))
     delta = np.empty((B, H, Lq))
     rc = _load().fa2_oracle_bwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, do.ctypes.data, B, H, Lq, Lk, D,
-                                     int(bool(causal)), float(scale), dq.ctypes.data, dk.ctypes.data,
+                                     int(bool(causal)), _window_arg(causal, window, Lq, Lk), float(scale),
+                                     dq.ctypes.data, dk.ctypes.data,
                                      dv.ctypes.data, delta.ctypes.data, int(threads))
     if rc != 0:
         raise RuntimeError(f"fa2_oracle_bwd_f64 failed with code {rc}")
     return dq, dk, dv, delta
 
 
-def gradients(q, k, v, do, causal: bool, scale: float, heads=None, threads: int = 0):
+def gradients(q, k, v, do, causal: bool, scale: float, heads=None, threads: int = 0, window=None):
     """Backward definition for bf16 inputs (torch tensors, widened exactly to fp64).
 
     heads: optional list of flat head ids b*H + h to compute (default: all); the
@@ -199,7 +220,8 @@ def gradients(q, k, v, do, causal: bool, scale: float, heads=None, threads: int 
         idx = np.asarray(heads, dtype=np.int64)
         arrs = [a[idx] for a in arrs]
     n = arrs[0].shape[0]
-    dq, dk, dv, delta = gradients_f64(*(a.reshape(1, n, a.shape[1], D) for a in arrs), causal, scale, threads)
+    dq, dk, dv, delta = gradients_f64(*(a.reshape(1, n, a.shape[1], D) for a in arrs), causal, scale, threads,
+                                      window)
     if heads is None:
         return (dq.reshape(B, H, Lq, D), dk.reshape(B, H, Lk, D), dv.reshape(B, H, Lk, D), delta.reshape(B, H, Lq))
     return dq[0], dk[0], dv[0], delta[0]

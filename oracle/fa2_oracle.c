@@ -63,10 +63,15 @@ void fa2_oracle_decode_bf16(const uint16_t *src, double *dst, int64_t n)
         dst[t] = bf16_to_f64(src[t]);
 }
 
-/* Key j is visible to query i (causal mask of chapter 08, section 4). */
-static int allowed(int64_t i, int64_t j, int causal)
+/*
+ * Key j is visible to query i: the causal mask of chapter 08, section 4 (j <= i),
+ * and, with window >= 0, the sliding window of "Flash Attention: principles and
+ * implementation" (tbr8.org), section 6.3 -- window_size = (w, 0) with causal:
+ * w keys to the left of the query and none to the right, i.e. i - w <= j <= i.
+ */
+static int allowed(int64_t i, int64_t j, int causal, int64_t window)
 {
-    return !causal || j <= i;
+    return (!causal || j <= i) && (window < 0 || j >= i - window);
 }
 
 /*
@@ -75,14 +80,14 @@ static int allowed(int64_t i, int64_t j, int causal)
  */
 static int64_t one_row(const uint16_t *q_row, const uint16_t *k_head,
                        const uint16_t *v_head, int64_t i, int64_t Lk,
-                       int64_t D, int causal, double scale, double *s,
+                       int64_t D, int causal, int64_t window, double scale, double *s,
                        double *p, double *o_row, double *lse_out)
 {
     /* S row: s_j = scale * sum_d q_id k_jd  (fp64, inputs widened exactly). */
     int64_t n_allowed = 0;
     double m = -INFINITY;
     for (int64_t j = 0; j < Lk; ++j) {
-        if (!allowed(i, j, causal)) {
+        if (!allowed(i, j, causal, window)) {
             s[j] = -INFINITY; /* not in A_i; never read below */
             continue;
         }
@@ -99,7 +104,7 @@ static int64_t one_row(const uint16_t *q_row, const uint16_t *k_head,
     /* P row: p_j = exp(s_j - M) / sum_{A_i} exp(s_j - M);  p_j = 0 off A_i. */
     double z = 0.0;
     for (int64_t j = 0; j < Lk; ++j) {
-        if (allowed(i, j, causal)) {
+        if (allowed(i, j, causal, window)) {
             p[j] = exp(s[j] - m);
             z += p[j];
         } else {
@@ -113,7 +118,7 @@ static int64_t one_row(const uint16_t *q_row, const uint16_t *k_head,
     for (int64_t d = 0; d < D; ++d)
         o_row[d] = 0.0;
     for (int64_t j = 0; j < Lk; ++j) {
-        if (!allowed(i, j, causal))
+        if (!allowed(i, j, causal, window))
             continue;
         const uint16_t *v_row = v_head + j * D;
         for (int64_t d = 0; d < D; ++d)
@@ -136,11 +141,11 @@ static int64_t one_row(const uint16_t *q_row, const uint16_t *k_head,
  *
  * Returns 0 on success, 1 on a bad argument, 2 on allocation failure.
  */
-int fa2_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                    int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t D,
-                    int causal, double scale, const int64_t *rows,
-                    int64_t n_rows, double *o, double *lse, double *p_out,
-                    int n_threads)
+int fa2_oracle_rows_w(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t D,
+                      int causal, int64_t window, double scale, const int64_t *rows,
+                      int64_t n_rows, double *o, double *lse, double *p_out,
+                      int n_threads)
 {
     if (!q || !k || !v || !o || !lse || (n_rows > 0 && !rows))
         return 1;
@@ -173,7 +178,7 @@ int fa2_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 const uint16_t *q_row = q + (bh * Lq + i) * D;
                 const uint16_t *k_head = k + bh * Lk * D;
                 const uint16_t *v_head = v + bh * Lk * D;
-                one_row(q_row, k_head, v_head, i, Lk, D, causal, scale, s, p,
+                one_row(q_row, k_head, v_head, i, Lk, D, causal, window, scale, s, p,
                         o + r * D, lse + r);
                 if (p_out)
                     memcpy(p_out + r * Lk, p, (size_t)Lk * sizeof(double));
@@ -215,13 +220,13 @@ int fa2_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 
 /* fp64 forward for fp64 inputs (contiguous (B, H, L, D)); same row definition. */
 static int64_t one_row_f64(const double *q_row, const double *k_head, const double *v_head, int64_t i,
-                           int64_t Lk, int64_t D, int causal, double scale, double *s, double *p,
+                           int64_t Lk, int64_t D, int causal, int64_t window, double scale, double *s, double *p,
                            double *o_row, double *lse_out)
 {
     int64_t n_allowed = 0;
     double m = -INFINITY;
     for (int64_t j = 0; j < Lk; ++j) {
-        if (!allowed(i, j, causal)) {
+        if (!allowed(i, j, causal, window)) {
             s[j] = -INFINITY;
             continue;
         }
@@ -235,7 +240,7 @@ static int64_t one_row_f64(const double *q_row, const double *k_head, const doub
     }
     double z = 0.0;
     for (int64_t j = 0; j < Lk; ++j) {
-        if (allowed(i, j, causal)) {
+        if (allowed(i, j, causal, window)) {
             p[j] = exp(s[j] - m);
             z += p[j];
         } else {
@@ -247,7 +252,7 @@ static int64_t one_row_f64(const double *q_row, const double *k_head, const doub
     for (int64_t d = 0; d < D; ++d)
         o_row[d] = 0.0;
     for (int64_t j = 0; j < Lk; ++j) {
-        if (!allowed(i, j, causal))
+        if (!allowed(i, j, causal, window))
             continue;
         for (int64_t d = 0; d < D; ++d)
             o_row[d] += p[j] * v_head[j * D + d];
@@ -262,7 +267,8 @@ static int64_t one_row_f64(const double *q_row, const double *k_head, const doub
  * fa2_oracle_rows.
  */
 int fa2_oracle_fwd_f64(const double *q, const double *k, const double *v, int64_t B, int64_t H, int64_t Lq,
-                       int64_t Lk, int64_t D, int causal, double scale, double *o, double *lse, int n_threads)
+                       int64_t Lk, int64_t D, int causal, int64_t window, double scale, double *o, double *lse,
+                       int n_threads)
 {
     if (!q || !k || !v || !o || !lse || B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0)
         return 1;
@@ -284,7 +290,7 @@ int fa2_oracle_fwd_f64(const double *q, const double *k, const double *v, int64_
 #pragma omp for schedule(dynamic, 8)
             for (int64_t r = 0; r < B * H * Lq; ++r) {
                 const int64_t bh = r / Lq, i = r % Lq;
-                one_row_f64(q + r * D, k + bh * Lk * D, v + bh * Lk * D, i, Lk, D, causal, scale, s, p,
+                one_row_f64(q + r * D, k + bh * Lk * D, v + bh * Lk * D, i, Lk, D, causal, window, scale, s, p,
                             o + r * D, lse + r);
             }
         }
@@ -296,8 +302,8 @@ int fa2_oracle_fwd_f64(const double *q, const double *k, const double *v, int64_
 
 /* Gradients of one head (all fp64); s, p, dp: scratch rows of Lk; o_row: D. */
 static void one_head_bwd(const double *q, const double *k, const double *v, const double *dout, int64_t Lq,
-                         int64_t Lk, int64_t D, int causal, double scale, double *dq, double *dk, double *dv,
-                         double *delta, double *s, double *p, double *dp, double *o_row)
+                         int64_t Lk, int64_t D, int causal, int64_t window, double scale, double *dq, double *dk,
+                         double *dv, double *delta, double *s, double *p, double *dp, double *o_row)
 {
     for (int64_t t = 0; t < Lk * D; ++t) {
         dk[t] = 0.0;
@@ -306,7 +312,7 @@ static void one_head_bwd(const double *q, const double *k, const double *v, cons
     for (int64_t i = 0; i < Lq; ++i) {
         const double *q_row = q + i * D, *do_row = dout + i * D;
         double lse;
-        one_row_f64(q_row, k, v, i, Lk, D, causal, scale, s, p, o_row, &lse);
+        one_row_f64(q_row, k, v, i, Lk, D, causal, window, scale, s, p, o_row, &lse);
         /* Delta_i = dO_i . O_i */
         double dl = 0.0;
         for (int64_t d = 0; d < D; ++d)
@@ -315,7 +321,7 @@ static void one_head_bwd(const double *q, const double *k, const double *v, cons
             delta[i] = dl;
         /* dP row, then dS row (kept in dp) */
         for (int64_t j = 0; j < Lk; ++j) {
-            if (!allowed(i, j, causal)) {
+            if (!allowed(i, j, causal, window)) {
                 dp[j] = 0.0;
                 continue;
             }
@@ -329,7 +335,7 @@ static void one_head_bwd(const double *q, const double *k, const double *v, cons
         for (int64_t d = 0; d < D; ++d)
             dq_row[d] = 0.0;
         for (int64_t j = 0; j < Lk; ++j) {
-            if (!allowed(i, j, causal))
+            if (!allowed(i, j, causal, window))
                 continue;
             for (int64_t d = 0; d < D; ++d) {
                 dq_row[d] += dp[j] * k[j * D + d];
@@ -349,8 +355,8 @@ static void one_head_bwd(const double *q, const double *k, const double *v, cons
  * D); delta (B, H, Lq) optional.  Returns as fa2_oracle_rows.
  */
 int fa2_oracle_bwd_f64(const double *q, const double *k, const double *v, const double *dout, int64_t B,
-                       int64_t H, int64_t Lq, int64_t Lk, int64_t D, int causal, double scale, double *dq,
-                       double *dk, double *dv, double *delta, int n_threads)
+                       int64_t H, int64_t Lq, int64_t Lk, int64_t D, int causal, int64_t window, double scale,
+                       double *dq, double *dk, double *dv, double *delta, int n_threads)
 {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0)
         return 1;
@@ -374,7 +380,7 @@ int fa2_oracle_bwd_f64(const double *q, const double *k, const double *v, const 
 #pragma omp for schedule(dynamic, 1)
             for (int64_t bh = 0; bh < B * H; ++bh)
                 one_head_bwd(q + bh * Lq * D, k + bh * Lk * D, v + bh * Lk * D, dout + bh * Lq * D, Lq, Lk, D,
-                             causal, scale, dq + bh * Lq * D, dk + bh * Lk * D, dv + bh * Lk * D,
+                             causal, window, scale, dq + bh * Lq * D, dk + bh * Lk * D, dv + bh * Lk * D,
                              delta ? delta + bh * Lq : NULL, s, p, dp, o_row);
         }
         free(s);
@@ -383,6 +389,17 @@ int fa2_oracle_bwd_f64(const double *q, const double *k, const double *v, const 
         free(o_row);
     }
     return failed ? 2 : 0;
+}
+
+/* fa2_oracle_rows_w without a window. */
+int fa2_oracle_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t D,
+                    int causal, double scale, const int64_t *rows,
+                    int64_t n_rows, double *o, double *lse, double *p_out,
+                    int n_threads)
+{
+    return fa2_oracle_rows_w(q, k, v, B, H, Lq, Lk, D, causal, -1, scale, rows, n_rows, o, lse, p_out,
+                             n_threads);
 }
 
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
