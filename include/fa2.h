@@ -77,6 +77,24 @@ fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o,
                    int causal, float scale, void *stream);
 
 /*
+ * fa2_fwd_window -- fa2_fwd for causal attention restricted to a sliding
+ * window: query i sees keys i - window <= j <= i ("Flash Attention:
+ * principles and implementation" (tbr8.org), section 6.3, window_size =
+ * (window, 0) with causal=True: `window` keys to the left, none to the right).
+ * K/V tiles entirely left of a query tile's band are never visited, so the
+ * work grows as Lq * window instead of Lq * Lk / 2.
+ *
+ *   window   >= 0 (0: each query sees only its own key; >= Lk: plain causal).
+ *   Lq <= Lk is required (every row keeps key i).
+ *   (other arguments as for fa2_fwd)
+ *
+ * Errors: as fa2_fwd; FA2_ERR_INVALID_ARG for window < 0 or Lq > Lk.
+ */
+fa2_status fa2_fwd_window(const void *q, const void *k, const void *v, void *o,
+                          float *lse, int B, int H, int Lq, int Lk, int D,
+                          int window, float scale, void *stream);
+
+/*
  * fa2_workspace_size -- bytes of device workspace fa2_fwd_ws needs for this
  * problem on `device` (its SM count sets the schedule).  *bytes = 0 when the
  * pass uses none: causal passes, Lq == 0, and non-causal shapes for which

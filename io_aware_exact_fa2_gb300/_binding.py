@@ -44,6 +44,8 @@ def load_library() -> ctypes.CDLL:
     lib.fa2_workspace_size.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.fa2_fwd_ws.restype = i
     lib.fa2_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.fa2_fwd_window.restype = i
+    lib.fa2_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa2_fwd_noalloc.restype = i
     lib.fa2_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa2_bwd_workspace_size.restype = i
@@ -131,6 +133,20 @@ def fa2_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=No
         where = "fa2_fwd_ws"
     if st != 0:
         raise Fa2Error(st, where)
+
+
+def fa2_fwd_window(q, k, v, o, lse, window: int, scale: float | None = None, stream=None) -> None:
+    """Causal forward restricted to the sliding window i - window <= j <= i (Lq <= Lk)."""
+    B, H, Lq, Lk, D = _check_shapes(q, k, v, o, lse)
+    for t in (q, k, v, o, lse):
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+    if scale is None:
+        scale = D ** -0.5
+    st = _lib.fa2_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             B, H, Lq, Lk, D, int(window), float(scale), _stream_handle(stream, q.device))
+    if st != 0:
+        raise Fa2Error(st, "fa2_fwd_window")
 
 
 def fa2_fwd_noalloc(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:

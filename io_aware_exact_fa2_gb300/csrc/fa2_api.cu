@@ -187,7 +187,7 @@ fa2_status select_device_of(const void *ptr, int *dev_out)
 
 fa2_status launch(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Lq,
                   int Lk, int D, int causal, float scale, cudaStream_t stream, void *workspace = nullptr,
-                  size_t workspace_bytes = 0)
+                  size_t workspace_bytes = 0, int window = -1)
 {
     int dev = 0;
     fa2_status st = select_device_of(q, &dev);
@@ -204,6 +204,7 @@ fa2_status launch(const void *q, const void *k, const void *v, void *o, float *l
     a.Lq = Lq;
     a.Lk = Lk;
     a.causal = causal;
+    a.window = window;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     a.err = device_error_ptr(dev);
     a.wait_limit_ns = wait_limit_ns();
@@ -373,6 +374,18 @@ FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const
     if (!a.err || !a.encode)
         return FA2_ERR_CUDA;
     return fa2::launch_bwd(a);
+}
+
+FA2_EXPORT fa2_status fa2_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                                     int H, int Lq, int Lk, int D, int window, float scale, void *stream)
+{
+    fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
+    if (st != FA2_OK || Lq == 0)
+        return st;
+    if (window < 0 || Lq > Lk)   // every row must keep its own key i
+        return FA2_ERR_INVALID_ARG;
+    return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, 1, scale, static_cast<cudaStream_t>(stream), nullptr, 0,
+                       window);
 }
 
 FA2_EXPORT fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,

@@ -57,6 +57,10 @@ struct FwdParams {
     int n_qgroups;              // ceil(Lq / (NQ * 128))
     int n_units;                // n_qgroups * BH
     int causal;
+    // causal sliding window: query i sees keys i - window <= j <= i (-1: none)
+    int window;
+    int unit_rows;              // NQ * 128 query rows per work unit
+    int kv_rows;                // BN rows per K/V tile
     float scale_log2;           // scale * log2(e), > 0
     // split schedule (non-causal, with a workspace): the n_units * n_kv K/V-tile
     // iterations are cut into gridDim.x contiguous ranges, one per CTA, of equal cost
@@ -251,6 +255,11 @@ __device__ __forceinline__ bool segment_at(int i, const FwdParams &p, const Spli
             return false;
         sg.unit = u;
         sg.kv_lo = 0;
+        if (p.window >= 0) {   // the unit's first K/V tile holding a key its first row may see
+            int qg, bh;
+            decode_unit(u, p, qg, bh);
+            sg.kv_lo = max(0, qg * p.unit_rows - p.window) / p.kv_rows;
+        }
         sg.kv_hi = 0x7fffffff;
         sg.slot = 0;
         sg.c_first = sg.c_last = static_cast<int>(blockIdx.x);
@@ -273,7 +282,7 @@ __device__ __forceinline__ bool segment_at(int i, const FwdParams &p, const Spli
 __device__ __forceinline__ int segment_tiles(const Segment &sg, int q0_t, const FwdParams &p, int BN)
 {
     if (!p.split)
-        return kv_tiles_for(q0_t, p.Lq, p.Lk, p.causal, BN);
+        return max(0, kv_tiles_for(q0_t, p.Lq, p.Lk, p.causal, BN) - sg.kv_lo);
     return q0_t < p.Lq ? sg.kv_hi - sg.kv_lo : 0;
 }
 
@@ -650,7 +659,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const int n = segment_tiles(sg, q0_t, p, C::BN);
             if (n == 0)
                 continue;
-            const int kv0 = p.split ? sg.kv_lo : 0;  // absolute index of the segment's first K/V tile
+            const int kv0 = sg.kv_lo;                // absolute index of the segment's first K/V tile
             if constexpr (C::QT) {
                 if (i == 0 && !(ok = copy_q()))
                     break;
@@ -685,14 +694,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                             s[32 * q + e] = __uint_as_float(r[q][e]);
                 }
 
-                // mask: key tail (j >= Lk) and, on tiles crossing the diagonal, causal j > i
+                // mask: key tail (j >= Lk), on tiles crossing the diagonal causal j > i, and
+                // on tiles crossing a sliding window's left edge j < i - window
                 const int jj = kv0 + j;                  // absolute K/V tile
                 const int k0 = jj * C::BN + h * C::NCOL;
-                if ((p.causal && jj * C::BN + C::BN - 1 > q0_t) || (jj * C::BN + C::BN > p.Lk)) {
+                const bool band_left = p.window >= 0 && jj * C::BN < q0_t + C::BM - 1 - p.window;
+                if ((p.causal && jj * C::BN + C::BN - 1 > q0_t) || (jj * C::BN + C::BN > p.Lk) || band_left) {
                     const int lim = p.causal ? min(grow + 1, p.Lk) : p.Lk;  // keys < lim are visible
+                    const int lo = p.window >= 0 ? grow - p.window : 0;      // and keys >= lo
 #pragma unroll
                     for (int c = 0; c < C::NCOL; ++c)
-                        if (k0 + c >= lim)
+                        if (k0 + c >= lim || k0 + c < lo)
                             s[c] = -INFINITY;
                 }
 
@@ -724,10 +736,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 }
                 const float m_tile = mx * c2;
 
-                // The first tile of a segment always holds a key every row may see (key 0
-                // for whole units; any tile for the non-causal split schedule), so m_tile
-                // is finite there; later tiles keep the stale max unless it grows a lot.
-                // All slices of a row see the same m_tile and so take the same decision.
+                // The first tile of a segment holds a key every row may see (key 0 for whole
+                // units; any tile for the non-causal split schedule) except under a sliding
+                // window, where a row's first visible key may come later: its max is then
+                // -inf until it does, and the first finite max replaces it through a
+                // rescale by 2^-inf = 0.  Later tiles keep the stale max unless it grows a
+                // lot.  All slices of a row see the same m_tile and so take the same decision.
                 float alpha = 1.f;
                 bool rescale = false;
                 if (j == 0) {
@@ -747,7 +761,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 // of its weight then cancels instead of showing up in O.
                 // (scale and subtract, and the exact sum, run as packed fp32 pairs)
                 const uint64_t c2x2 = f32x2(c2, c2);
-                const uint64_t negm2 = f32x2(-m_use, -m_use);
+                // a row may see no key of a window's first tile: its max is then -inf and
+                // its weights are 2^-inf = 0 with any finite base
+                const float m_sub = m_use == -INFINITY ? 0.f : m_use;
+                const uint64_t negm2 = f32x2(-m_sub, -m_sub);
                 uint64_t ls01 = 0, ls23 = 0;   // packed (0.f, 0.f)
                 float lr0 = 0.f, lr1 = 0.f;
                 {

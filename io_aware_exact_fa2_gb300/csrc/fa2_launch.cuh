@@ -23,6 +23,7 @@ struct LaunchArgs {
     float *lse;
     int B, H, Lq, Lk;
     int causal;
+    int window;               // causal sliding window, -1: none
     float scale_log2;
     int *err;
     unsigned long long wait_limit_ns;
@@ -115,6 +116,9 @@ fa2_status launch_fwd(const LaunchArgs &a)
     p.BH = BH;
     p.n_qgroups = (a.Lq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
     p.causal = a.causal ? 1 : 0;
+    p.window = a.window;
+    p.unit_rows = C::NQ * C::BM;
+    p.kv_rows = C::BN;
     p.scale_log2 = a.scale_log2;
     const long long units = static_cast<long long>(p.n_qgroups) * BH;
     if (units > INT_MAX)

@@ -33,8 +33,8 @@ def header_functions():
 
 def test_header_declares_the_boundary():
     assert header_functions() == ["fa2_bwd", "fa2_bwd_workspace_size", "fa2_fwd", "fa2_fwd_from_host",
-                                  "fa2_fwd_noalloc", "fa2_fwd_ws", "fa2_get_device_error", "fa2_status_string",
-                                  "fa2_version", "fa2_workspace_size"]
+                                  "fa2_fwd_noalloc", "fa2_fwd_window", "fa2_fwd_ws", "fa2_get_device_error",
+                                  "fa2_status_string", "fa2_version", "fa2_workspace_size"]
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -163,3 +163,13 @@ def test_bwd_validation(lib):
     assert call_bwd(ws_bytes=4) == INVALID
     assert call_bwd(D=256) == UNSUPPORTED
     assert call_bwd(scale=float("nan")) == INVALID
+
+
+def test_window_validation(lib):
+    """fa2_fwd_window rejects a negative window and Lq > Lk before any CUDA call."""
+    f = lib.fa2_fwd_window
+    assert f(P, P, P, P, P, 1, 1, 8, 8, 64, -1, 0.125, None) == INVALID
+    assert f(P, P, P, P, P, 1, 1, 9, 8, 64, 4, 0.125, None) == INVALID
+    assert f(0, P, P, P, P, 1, 1, 8, 8, 64, 4, 0.125, None) == INVALID
+    assert f(P, P, P, P, P, 1, 1, 8, 8, 96, 4, 0.125, None) == UNSUPPORTED
+    assert f(P, P, P, P, P, 1, 1, 0, 8, 64, 4, 0.125, None) == OK   # Lq == 0: no-op

@@ -1,0 +1,95 @@
+"""Causal sliding-window forward ("Flash Attention: principles and implementation",
+section 6.3: window_size = (w, 0) with causal) on the GPU against the oracle.
+
+Tolerance, from the arithmetic.  The kernel weighs the values with bf16-rounded
+probabilities p~_j = p_j (1 + e_j), |e_j| <= 2^-9, and divides by their sum, so
+each normalised weight moves by at most ~2^-8 of itself and
+|dO_id| <= 2^-8 * max_{j visible} |v_jd - O_id|; storing O in bf16 adds up to
+2^-9 |O_id|.  With thousands of keys per row the errors average out far below
+the forward workloads' 1e-2, but a narrow window leaves only a few keys per row
+(w = 1: two), where the bound itself exceeds 1e-2.  So every element must meet
+|dO| <= 2^-8 * max_j |v_jd - O_id| + 2^-8 |O_id| + 1e-5, and LSE the forward's
+1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from io_aware_exact_fa2_gb300.workloads import make_qkv
+from parity import sample_rows, scale_of
+
+pytestmark = pytest.mark.gpu
+
+
+def compare(o, lse, o_ref, lse_ref, v, window, Lq, rows=None):
+    """o, lse: GPU results for the flat rows `rows` (bh * Lq + i; all rows when None),
+    o_ref, lse_ref: the oracle's for the same rows; v: the bf16 values."""
+    B, H, Lk, D = v.shape
+    vf = v.double().numpy().reshape(B * H, Lk, D)
+    og = o.double().numpy().reshape(-1, D)
+    lg = lse.double().numpy().reshape(-1)
+    orf = np.asarray(o_ref).reshape(-1, D)
+    lrf = np.asarray(lse_ref).reshape(-1)
+    if rows is None:
+        rows = np.arange(og.shape[0])
+    assert np.isfinite(og).all() and np.isfinite(lg).all()
+    assert np.max(np.abs(lg - lrf)) <= 1e-3
+    for n, r in enumerate(rows):
+        bh, i = divmod(int(r), Lq)
+        lo, hi = max(0, i - window), min(i, Lk - 1)
+        spread = np.max(np.abs(vf[bh, lo:hi + 1] - orf[n]), axis=0)
+        bound = 2.0 ** -8 * spread + 2.0 ** -8 * np.abs(orf[n]) + 1e-5
+        err = np.abs(og[n] - orf[n])
+        assert np.all(err <= bound), (int(r), float(np.max(err - bound)))
+
+
+def run_window(q, k, v, window, scale):
+    from io_aware_exact_fa2_gb300 import fa2_fwd_window, fa2_get_device_error
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    B, H, Lq, D = q.shape
+    o = torch.full((B, H, Lq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((B, H, Lq), float("nan"), dtype=torch.float32, device=dev)
+    fa2_fwd_window(qd, kd, vd, o, lse, window, scale)
+    st, code = fa2_get_device_error()
+    assert st == 0, f"device error {code:#x}"
+    return o.cpu(), lse.cpu()
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("window", [0, 1, 100, 128, 255, 700])
+def test_window_every_element(D, window):
+    """Windows narrower than, equal to and wider than a K/V tile, on ragged shapes
+    whose query tiles start inside and outside the band's left edge."""
+    q, k, v = make_qkv(2, 2, 600, 600, D, seed_base=9000 + D + window)
+    o, lse = run_window(q, k, v, window, scale_of(D))
+    o_ref, lse_ref = oracle.attention(q, k, v, True, scale_of(D), window=window)
+    compare(o, lse, o_ref, lse_ref, v, window, 600)
+
+
+@pytest.mark.parametrize("Lq,Lk", [(300, 457), (1, 9), (129, 130)])
+def test_window_fewer_queries_than_keys(Lq, Lk):
+    q, k, v = make_qkv(1, 3, Lq, Lk, 128, seed_base=9100 + Lq)
+    o, lse = run_window(q, k, v, 64, scale_of(128))
+    o_ref, lse_ref = oracle.attention(q, k, v, True, scale_of(128), window=64)
+    compare(o, lse, o_ref, lse_ref, v, 64, Lq)
+
+
+def test_wide_window_is_plain_causal_bit_for_bit():
+    from parity import run_cuda
+    q, k, v = make_qkv(2, 4, 700, 700, 128, seed_base=9200)
+    o_w, l_w = run_window(q, k, v, 700, scale_of(128))
+    o_c, l_c = run_cuda(q, k, v, True, scale_of(128))
+    assert torch.equal(o_w, o_c) and torch.equal(l_w, l_c)
+
+
+def test_window_at_the_forward_bench_size():
+    """B2 H16 L4096 D128 with a 1024-key window: sampled rows (tile edges + random)."""
+    B, H, L, D, w = 2, 16, 4096, 128, 1024
+    q, k, v = make_qkv(B, H, L, L, D, seed_base=9300)
+    o, lse = run_window(q, k, v, w, scale_of(D))
+    rows = sample_rows(B, H, L, n_random=512, seed=9301)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, True, scale_of(D), rows, window=w)
+    idx = torch.from_numpy(rows)
+    compare(o.reshape(-1, D)[idx], lse.reshape(-1)[idx], o_ref, lse_ref, v, w, L, rows=rows)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
