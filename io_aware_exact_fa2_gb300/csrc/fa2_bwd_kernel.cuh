@@ -264,14 +264,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok)
                     break;
-                // row statistics of this query tile: lse2 (+inf past Lq, so P = 0 there)
-                // and Delta (0 past Lq)
+                // row statistics of this query tile, negated for the FMAs that use them:
+                // -lse2 (-inf past Lq, so P = 0 there) and -Delta (0 past Lq)
                 const int q0 = (qt0 + s) * C::STR;
                 float *stat = reinterpret_cast<float *>(sgen + C::OFF_STAT + st * 2 * C::STR * 4);
                 for (int r = lane; r < C::STR; r += 32) {
                     const int qi = q0 + r;
-                    stat[r] = qi < p.Lq ? lse_h[qi] * BWD_LOG2E : INFINITY;
-                    stat[C::STR + r] = qi < p.Lq ? delta_h[qi] : 0.f;
+                    stat[r] = qi < p.Lq ? -lse_h[qi] * BWD_LOG2E : -INFINITY;
+                    stat[C::STR + r] = qi < p.Lq ? -delta_h[qi] : 0.f;
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -404,34 +404,55 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 break;
             const uint32_t a_st = tmem + lane_base + TM_ST + b * C::STR;
             const uint32_t a_dp = tmem + lane_base + TM_DPT + b * C::STR;
-            const float *stat = reinterpret_cast<const float *>(sgen + C::OFF_STAT + st * 2 * C::STR * 4);
+            const uint32_t stat = sbase + C::OFF_STAT + st * 2 * C::STR * 4;
             const int q0 = (qt0 + s) * C::STR;
-            // query columns c with q0 + c < kj are masked (causal, key after query)
-            const int first_visible = p.causal ? kj - q0 : 0;
+            // query columns c < kj - q0 are masked (causal, key after query); only tiles
+            // reaching below some of this warp's keys need it
+            const int first_visible = kj - q0;
+            const bool need_mask = p.causal && q0 < k0 + warp * 32 + 31;
+            const uint64_t c2x2 = f32x2(c2, c2);
+            const uint64_t zero2 = 0;
             uint32_t pw[C::STR / 2], dw[C::STR / 2];
 #pragma unroll
             for (int ch = 0; ch < C::STR / 32; ++ch) {
                 uint32_t rs[32], rd[32];
                 tmem_ld32(a_st + 32 * ch, rs);
                 tmem_ld32(a_dp + 32 * ch, rd);
+                // this chunk's -lse2 and -Delta (same for every lane: broadcast loads)
+                uint32_t nl[32], nd[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    ld_shared_v4(stat + (32 * ch + 4 * q) * 4, nl[4 * q], nl[4 * q + 1], nl[4 * q + 2], nl[4 * q + 3]);
+                    ld_shared_v4(stat + (C::STR + 32 * ch + 4 * q) * 4, nd[4 * q], nd[4 * q + 1], nd[4 * q + 2],
+                                 nd[4 * q + 3]);
+                }
                 tmem_ld_wait(rs);
                 tmem_ld_wait(rd);
+                float pv[32], dv[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const int c = 32 * ch + e;
-                    float pv[2], dv[2];
+                    float x0, x1;
+                    unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2x2,
+                                           f32x2(__uint_as_float(nl[e]), __uint_as_float(nl[e + 1]))),
+                                 x0, x1);
+                    pv[e] = ex2_approx(x0);
+                    pv[e + 1] = ex2_approx(x1);
+                    const uint64_t diff = add_f32x2(f32x2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])),
+                                                    f32x2(__uint_as_float(nd[e]), __uint_as_float(nd[e + 1])));
+                    unpack_f32x2(fma_f32x2(f32x2(pv[e], pv[e + 1]), diff, zero2), dv[e], dv[e + 1]);
+                }
+                if (need_mask) {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const float lse2 = stat[c + u];
-                        const float dl = stat[C::STR + c + u];
-                        float pp = ex2_approx(fmaf(__uint_as_float(rs[e + u]), c2, -lse2));
-                        if (c + u < first_visible)
-                            pp = 0.f;
-                        pv[u] = pp;
-                        dv[u] = pp * (__uint_as_float(rd[e + u]) - dl);
-                    }
-                    pw[c / 2] = bwd_pack(pv[0], pv[1]);
-                    dw[c / 2] = bwd_pack(dv[0], dv[1]);
+                    for (int e = 0; e < 32; ++e)
+                        if (32 * ch + e < first_visible) {
+                            pv[e] = 0.f;
+                            dv[e] = 0.f;
+                        }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    pw[(32 * ch + e) / 2] = bwd_pack(pv[e], pv[e + 1]);
+                    dw[(32 * ch + e) / 2] = bwd_pack(dv[e], dv[e + 1]);
                 }
             }
             // P^T and dS^T as bf16 pairs over the first STR/2 columns of their buffers
@@ -668,7 +689,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const uint32_t a_s = tmem + lane_base + TM_S + b * C::STR;
             const uint32_t a_dp = tmem + lane_base + TM_DP + b * C::STR;
             const int j0 = s * C::STR;
-            const bool masked = j0 + C::STR > lim;
+            // key columns at or past lim are masked; only a tile reaching lim for some
+            // row of this warp needs the per-element test
+            const bool need_mask = __any_sync(0xffffffffu, j0 + C::STR > lim);
+            const uint64_t c2x2 = f32x2(c2, c2);
+            const uint64_t nl2 = f32x2(-lse2, -lse2);
+            const uint64_t nd2 = f32x2(-dl, -dl);
+            const uint64_t zero2 = 0;
             uint32_t dw[C::STR / 2];
 #pragma unroll
             for (int ch = 0; ch < C::STR / 32; ++ch) {
@@ -677,18 +704,25 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 tmem_ld32(a_dp + 32 * ch, rd);
                 tmem_ld_wait(rs);
                 tmem_ld_wait(rd);
+                float dv[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float dv[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        float pp = ex2_approx(fmaf(__uint_as_float(rs[e + u]), c2, -lse2));
-                        if (masked && j0 + 32 * ch + e + u >= lim)
-                            pp = 0.f;
-                        dv[u] = pp * (__uint_as_float(rd[e + u]) - dl);
-                    }
-                    dw[(32 * ch + e) / 2] = bwd_pack(dv[0], dv[1]);
+                    float x0, x1;
+                    unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2x2, nl2), x0,
+                                 x1);
+                    const uint64_t pp = f32x2(ex2_approx(x0), ex2_approx(x1));
+                    const uint64_t diff = add_f32x2(f32x2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])), nd2);
+                    unpack_f32x2(fma_f32x2(pp, diff, zero2), dv[e], dv[e + 1]);
                 }
+                if (need_mask) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (j0 + 32 * ch + e >= lim)
+                            dv[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 32; e += 2)
+                    dw[(32 * ch + e) / 2] = bwd_pack(dv[e], dv[e + 1]);
             }
             if constexpr (C::STR / 2 >= 32) {
 #pragma unroll
