@@ -19,6 +19,14 @@
 //     units are ordered heaviest first and dealt out in a snake so heavy and
 //     light units pair up.  All barrier phases run on across units, so the next
 //     unit's Q and K/V tiles stream in while the current unit finishes.
+//     Non-causal passes given a workspace may instead cut the K/V-tile
+//     iterations of all units into one cost-balanced range per CTA (ranges
+//     planned on the host); a unit cut between CTAs is computed in parts that
+//     the last part to finish merges exactly (the online-softmax merge of two
+//     key blocks).  A causal sliding window starts each unit at the first K/V
+//     tile of its band.
+//   * Optionally (QT, one Q tile per unit) the softmax warps copy each Q tile
+//     from shared memory into TMEM, so S = Q K^T reads A from TMEM.
 //   * TMA (cp.async.bulk.tensor, 128B swizzle) moves Q (per unit) and K/V (per
 //     tile) into shared memory: a Q buffer per Q tile, refilled as soon as the
 //     last S MMA that reads it completes, and a KS-stage K/V ring.
