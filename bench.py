@@ -387,7 +387,6 @@ def run_ours(args, world, rank, local):
             "kernels": "Delta, dQ (query tiles resident), dK/dV (key tiles resident) per call (fa2_bwd)",
             "l2": "flushed (256 MiB write) before every timed call"}
     print(json.dumps(line), flush=True)
-    print(json.dumps(line), flush=True)
 
 
 def main():

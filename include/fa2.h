@@ -184,8 +184,9 @@ fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
                            int causal, float scale, void *stream);
 
 /*
- * fa2_bwd_workspace_size -- bytes of device workspace fa2_bwd needs: one fp32
- * per query row (Delta).  Returns FA2_OK; FA2_ERR_INVALID_ARG for bad sizes;
+ * fa2_bwd_workspace_size -- bytes of device workspace fa2_bwd needs: two fp32
+ * per query row (-lse * log2 e and -Delta), rows padded to a multiple of 32
+ * per head.  Returns FA2_OK; FA2_ERR_INVALID_ARG for bad sizes;
  * FA2_ERR_UNSUPPORTED for D other than 64 or 128.
  */
 fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, size_t *bytes);

@@ -315,7 +315,7 @@ FA2_EXPORT fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D
         return FA2_ERR_INVALID_ARG;
     if (D != 64 && D != 128)
         return FA2_ERR_UNSUPPORTED;
-    *bytes = fa2::align256(static_cast<size_t>(B) * H * Lq * sizeof(float));
+    *bytes = fa2::align256(fa2::bwd_stats_bytes(B, H, Lq));
     return FA2_OK;
 }
 
@@ -334,7 +334,7 @@ FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const
     if (!fa2::aligned(dout, 16) || !fa2::aligned(dq, 16) || !fa2::aligned(dk, 16) || !fa2::aligned(dv, 16) ||
         (workspace && !fa2::aligned(workspace, 16)))
         return FA2_ERR_INVALID_ARG;
-    if (workspace_bytes < static_cast<size_t>(B) * H * Lq * sizeof(float))
+    if (workspace_bytes < fa2::bwd_stats_bytes(B, H, Lq))
         return FA2_ERR_INVALID_ARG;
     int dev = 0;
     if ((st = fa2::select_device_of(q, &dev)) != FA2_OK)
@@ -355,7 +355,7 @@ FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const
     a.o = o;
     a.dout = dout;
     a.lse = lse;
-    a.delta = static_cast<float *>(workspace);
+    a.stats = static_cast<float *>(workspace);
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;

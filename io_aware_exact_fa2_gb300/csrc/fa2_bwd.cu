@@ -16,6 +16,7 @@ template <int D>
 using BwdKV = BwdCfg<D, 128, 32, 4>;
 template <int D>
 using BwdQ = BwdCfg<D, 128, 64, 3>;
+static_assert(BWD_STAT_TILE_ROWS == BWD_STAT_ROWS, "workspace sizing and kernels agree on the statistics tiles");
 
 template <class K>
 static bool set_smem(K kernel, int bytes, int device, std::atomic<unsigned long long> &configured)
@@ -48,8 +49,9 @@ static fa2_status launch_bwd_d(const BwdArgs &a)
         !encode_bhld(a.encode, &do_str, a.dout, D, a.Lq, BH, CKV::STR))
         return FA2_ERR_CUDA;
     BwdParams p;
-    p.lse = a.lse;
-    p.delta = a.delta;
+    const int n_stat_tiles = (a.Lq + BWD_STAT_ROWS - 1) / BWD_STAT_ROWS;
+    p.stats = a.stats;
+    p.n_stat_tiles = n_stat_tiles;
     p.dq = static_cast<uint16_t *>(a.dq);
     p.dk = static_cast<uint16_t *>(a.dk);
     p.dv = static_cast<uint16_t *>(a.dv);
@@ -67,9 +69,10 @@ static fa2_status launch_bwd_d(const BwdArgs &a)
         !set_smem(fa2_bwd_kv_kernel<CKV>, CKV::SMEM_BYTES, a.device, cfg_kv))
         return FA2_ERR_CUDA;
     if (a.Lq > 0) {
-        const long long rows = static_cast<long long>(BH) * a.Lq;
+        const long long rows = static_cast<long long>(BH) * n_stat_tiles * BWD_STAT_ROWS;
         fa2_bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(
-            static_cast<const uint16_t *>(a.o), static_cast<const uint16_t *>(a.dout), a.delta, rows);
+            static_cast<const uint16_t *>(a.o), static_cast<const uint16_t *>(a.dout), a.lse, a.stats, a.Lq,
+            n_stat_tiles, rows);
         const long long n_qt = (a.Lq + CQ::RES - 1) / CQ::RES;
         fa2_bwd_q_kernel<CQ><<<static_cast<unsigned>(n_qt * BH), CQ::NUM_THREADS, CQ::SMEM_BYTES, a.stream>>>(
             q_res, do_res, k_str, v_str, p);

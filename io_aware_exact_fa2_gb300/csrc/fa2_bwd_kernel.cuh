@@ -23,6 +23,10 @@
 //     over them as bf16 and read by the gradient MMAs straight from TMEM; the
 //     streamed tiles serve as the MMA's B operand both K-major (for S, dP) and
 //     MN-major (for dV, dK, dQ) without a transpose pass.
+//   * The Delta kernel also writes each query row's -lse * log2 e beside -Delta,
+//     in 32-row tiles, so a streamed query tile's statistics ride one bulk copy
+//     on the same ring barrier as its Q and dO tiles (no global loads in the
+//     producer's loop).
 //   * Every wait is bounded (a device error word records which one ran out).
 #pragma once
 
@@ -33,9 +37,15 @@
 
 namespace fa2 {
 
+// Per-row statistics the gradient kernels read, written by the Delta kernel in
+// tiles of BWD_STAT_ROWS query rows: fp32 [B*H][tiles][2][BWD_STAT_ROWS] holding
+// (-lse * log2 e, -Delta) per row, so that one bulk copy brings a streamed query
+// tile's statistics into shared memory.  Rows past Lq hold (-inf, 0): P = 0 there.
+constexpr int BWD_STAT_ROWS = 32;
+
 struct BwdParams {
-    const float *lse;       // fp32 [B*H, Lq], natural log (the forward's output)
-    const float *delta;     // fp32 [B*H, Lq]
+    const float *stats;     // the statistics tiles above
+    int n_stat_tiles;       // tiles per head = ceil(Lq / BWD_STAT_ROWS)
     uint16_t *dq;           // bf16 [B*H, Lq, D]
     uint16_t *dk, *dv;      // bf16 [B*H, Lk, D]
     int *err;
@@ -64,31 +74,44 @@ __device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, int
 }
 
 // ---------------------------------------------------------------- Delta (6.2)
-// One warp per query row: Delta = sum_d dO * O in fp32 from the bf16 tensors.
+// One warp per query row, padded rows included: Delta = sum_d dO * O in fp32 from
+// the bf16 tensors, stored negated beside -lse * log2 e in the statistics tiles.
 template <int D>
 __global__ void __launch_bounds__(256) fa2_bwd_delta_kernel(const uint16_t *__restrict__ o,
                                                             const uint16_t *__restrict__ dout,
-                                                            float *__restrict__ delta, long long rows)
+                                                            const float *__restrict__ lse,
+                                                            float *__restrict__ stats, int Lq, int n_tiles,
+                                                            long long rows)
 {
     const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows)
         return;
-    constexpr int PER = D / 32;   // elements per lane (2, 4 or 8)
-    const uint16_t *orow = o + r * D + lane * PER;
-    const uint16_t *drow = dout + r * D + lane * PER;
-    float acc = 0.f;
+    const long long per_head = static_cast<long long>(n_tiles) * BWD_STAT_ROWS;
+    const long long bh = r / per_head;
+    const int i = static_cast<int>(r - bh * per_head);
+    float acc = 0.f, neg_lse2 = -INFINITY;
+    if (i < Lq) {
+        const long long src = bh * Lq + i;
+        constexpr int PER = D / 32;   // elements per lane (2 or 4)
+        const uint16_t *orow = o + src * D + lane * PER;
+        const uint16_t *drow = dout + src * D + lane * PER;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-        const float a = __uint_as_float(static_cast<uint32_t>(orow[e]) << 16);
-        const float b = __uint_as_float(static_cast<uint32_t>(drow[e]) << 16);
-        acc = fmaf(a, b, acc);
+        for (int e = 0; e < PER; ++e) {
+            const float a = __uint_as_float(static_cast<uint32_t>(orow[e]) << 16);
+            const float b = __uint_as_float(static_cast<uint32_t>(drow[e]) << 16);
+            acc = fmaf(a, b, acc);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        neg_lse2 = -(lse[src] * BWD_LOG2E);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0)
-        delta[r] = acc;
+    if (lane == 0) {
+        float *t = stats + (bh * n_tiles + i / BWD_STAT_ROWS) * 2 * BWD_STAT_ROWS + i % BWD_STAT_ROWS;
+        t[0] = neg_lse2;
+        t[BWD_STAT_ROWS] = i < Lq ? -acc : 0.f;
+    }
 }
 
 // Shared configuration of the two gradient kernels: RES rows of the resident
@@ -110,8 +133,9 @@ struct BwdCfg {
     static constexpr int OFF_RES1 = RES_TILE;
     static constexpr int OFF_STR0 = 2 * RES_TILE;                 // [RING]
     static constexpr int OFF_STR1 = OFF_STR0 + RING * STR_TILE;    // [RING]
+    static constexpr int STAT_BYTES = 2 * STR * 4;                  // -lse2 and -Delta of STR rows
     static constexpr int OFF_STAT = OFF_STR1 + RING * STR_TILE;    // [RING][2][STR] f32
-    static constexpr int OFF_BAR = OFF_STAT + RING * 2 * STR * 4;
+    static constexpr int OFF_BAR = OFF_STAT + RING * STAT_BYTES;
     static constexpr int BAR_RES_FULL = 0;
     static constexpr int BAR_STR_FULL = 1;                  // [RING]
     static constexpr int BAR_STR_EMPTY = BAR_STR_FULL + RING;   // [RING]
@@ -188,6 +212,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                       const BwdParams p)
 {
     using namespace ptx;
+    static_assert(C::STR == BWD_STAT_ROWS, "one statistics tile per streamed query tile");
     // K and V are also copied into TMEM (TM_KA, TM_VA) so that S^T = K Q^T and
     // dP^T = V dO^T read their A operand from TMEM instead of loading it from
     // shared memory for every instruction
@@ -254,8 +279,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     tma_load_3d(sbase + C::OFF_RES1 + c * C::RES_BLOCK, &tm_v, 64 * c, k0, bh, bar(C::BAR_RES_FULL));
                 }
             }
-            const float *lse_h = p.lse + static_cast<size_t>(bh) * p.Lq;
-            const float *delta_h = p.delta + static_cast<size_t>(bh) * p.Lq;
+            // this head's statistics tiles from query tile qt0 on (-lse2 and -Delta,
+            // 2 * STR floats per tile, one bulk copy per step)
+            const float *stat_src = p.stats + (static_cast<size_t>(bh) * p.n_stat_tiles + qt0) * 2 * C::STR;
             for (int s = 0; s < n_steps && ok; ++s) {
                 const int st = s % C::RING;
                 if (s >= C::RING)
@@ -264,18 +290,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok)
                     break;
-                // row statistics of this query tile, negated for the FMAs that use them:
-                // -lse2 (-inf past Lq, so P = 0 there) and -Delta (0 past Lq)
                 const int q0 = (qt0 + s) * C::STR;
-                float *stat = reinterpret_cast<float *>(sgen + C::OFF_STAT + st * 2 * C::STR * 4);
-                for (int r = lane; r < C::STR; r += 32) {
-                    const int qi = q0 + r;
-                    stat[r] = qi < p.Lq ? -lse_h[qi] * BWD_LOG2E : -INFINITY;
-                    stat[C::STR + r] = qi < p.Lq ? -delta_h[qi] : 0.f;
-                }
-                __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(C::BAR_STR_FULL + st), 2 * C::STR_TILE);
+                    mbar_arrive_expect_tx(bar(C::BAR_STR_FULL + st), 2 * C::STR_TILE + C::STAT_BYTES);
+                    bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES, stat_src + s * 2 * C::STR, C::STAT_BYTES,
+                              bar(C::BAR_STR_FULL + st));
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c) {
                         tma_load_3d(sbase + C::OFF_STR0 + st * C::STR_TILE + c * C::STR_BLOCK, &tm_q, 64 * c, q0,
@@ -395,9 +414,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (!ok)
                 break;
             tc_fence_after();
-            // the row statistics were written by the producer warp before it armed
-            // this stage's barrier: acquire them from that barrier directly (it cannot
-            // have moved on, since the stage is only refilled after this step's MMAs)
+            // the row statistics arrive with the stage's tiles: wait on that barrier
+            // directly (it cannot have moved on, since the stage is only refilled
+            // after this step's MMAs)
             ok = warp_wait_all(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_ELEM | 5,
                                p.wait_limit_ns);
             if (!ok)
@@ -665,8 +684,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const float c2 = p.scale_log2;
         const bool live = qi < p.Lq;
         const size_t srow = static_cast<size_t>(bh) * p.Lq + (live ? qi : 0);
-        const float lse2 = live ? p.lse[srow] * BWD_LOG2E : INFINITY;
-        const float dl = live ? p.delta[srow] : 0.f;
+        const float *stat = p.stats +
+                            (static_cast<size_t>(bh) * p.n_stat_tiles + (live ? qi : 0) / BWD_STAT_ROWS) * 2 * BWD_STAT_ROWS +
+                            (live ? qi : 0) % BWD_STAT_ROWS;
+        const float lse2 = live ? -stat[0] : INFINITY;
+        const float dl = live ? -stat[BWD_STAT_ROWS] : 0.f;
         // keys j < lim are visible to this row
         const int lim = p.causal ? min(qi + 1, p.Lk) : p.Lk;
         // this row of Q and of dO into TMEM, as the score MMAs' A operands

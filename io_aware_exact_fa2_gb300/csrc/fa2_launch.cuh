@@ -164,7 +164,7 @@ fa2_status launch_fwd(const LaunchArgs &a)
 struct BwdArgs {
     const void *q, *k, *v, *o, *dout;
     const float *lse;
-    float *delta;             // workspace: B*H*Lq fp32
+    float *stats;             // workspace: per-row statistics tiles (bwd_stats_bytes)
     void *dq, *dk, *dv;
     int B, H, Lq, Lk, D;
     int causal;
@@ -176,6 +176,14 @@ struct BwdArgs {
     int device;
 };
 fa2_status launch_bwd(const BwdArgs &a);
+// Bytes of the backward's statistics tiles: two fp32 per query row, rows padded
+// to a multiple of BWD_STAT_TILE_ROWS per head.
+constexpr int BWD_STAT_TILE_ROWS = 32;
+constexpr size_t bwd_stats_bytes(int B, int H, int Lq)
+{
+    return static_cast<size_t>(B) * H * ((static_cast<size_t>(Lq) + BWD_STAT_TILE_ROWS - 1) / BWD_STAT_TILE_ROWS) *
+           BWD_STAT_TILE_ROWS * 2 * sizeof(float);
+}
 
 // One entry per head dimension (defined in fa2_fwd_d{64,128,256}.cu).
 fa2_status launch_fwd_d64(const LaunchArgs &a);
