@@ -10,12 +10,13 @@ namespace fa2 {
 
 // dK/dV: 128 keys resident, query tiles of 32 streamed through a 4-stage ring
 // (dV, dK, two 32-column score pairs and K, V as MMA operands fill TMEM);
-// dQ: 128 queries resident, key tiles of 64.  Two score buffer pairs let one
-// step's MMAs run while the previous step's elementwise work finishes.
+// dQ: 128 queries resident, key tiles of 64 through a 4-stage ring.  Two score
+// buffer pairs let one step's MMAs run while the previous step's elementwise
+// work finishes.
 template <int D>
-using BwdKV = BwdCfg<D, 128, 32, 4>;
+using BwdKV = BwdCfg<D, 128, 32, 4, 8>;
 template <int D>
-using BwdQ = BwdCfg<D, 128, 64, 3>;
+using BwdQ = BwdCfg<D, 128, 64, 4, 4>;
 static_assert(BWD_STAT_TILE_ROWS == BWD_STAT_ROWS, "workspace sizing and kernels agree on the statistics tiles");
 
 template <class K>

@@ -115,13 +115,16 @@ __global__ void __launch_bounds__(256) fa2_bwd_delta_kernel(const uint16_t *__re
 }
 
 // Shared configuration of the two gradient kernels: RES rows of the resident
-// tiles (TMEM lanes), STR rows per streamed tile, head dimension D.
-template <int D_, int RES_, int STR_, int RING_>
+// tiles (TMEM lanes), STR rows per streamed tile, head dimension D, EW
+// elementwise warps (4: one per 32-lane TMEM quarter; 8: two per quarter, each
+// with half of a step's columns).
+template <int D_, int RES_, int STR_, int RING_, int EW_>
 struct BwdCfg {
     static constexpr int D = D_;
     static constexpr int RES = RES_;     // resident rows per CTA (= 128 TMEM lanes)
     static constexpr int STR = STR_;     // rows of a streamed tile per step
     static constexpr int RING = RING_;   // streamed-tile ring stages
+    static constexpr int EW = EW_;       // elementwise warps
     static constexpr int DB = D / 64;    // 64-column (128-byte) swizzle blocks
     static constexpr int RES_BLOCK = RES * 128;
     static constexpr int RES_TILE = DB * RES_BLOCK;
@@ -139,20 +142,22 @@ struct BwdCfg {
     static constexpr int BAR_RES_FULL = 0;
     static constexpr int BAR_STR_FULL = 1;                  // [RING]
     static constexpr int BAR_STR_EMPTY = BAR_STR_FULL + RING;   // [RING]
-    static constexpr int BAR_PAIR_FULL = BAR_STR_EMPTY + RING;  // [2] score pair computed
-    static constexpr int BAR_PAIR_READY = BAR_PAIR_FULL + 2;    // [2] bf16 operands written
-    static constexpr int BAR_DONE = BAR_PAIR_READY + 2;         // every MMA completed
+    static constexpr int BAR_SCORE_FULL = BAR_STR_EMPTY + RING; // [2] a step's S^T and dP^T (dK/dV) or S (dQ)
+    static constexpr int BAR_DP_FULL = BAR_SCORE_FULL + 2;      // [2] a step's dP (dQ kernel)
+    static constexpr int BAR_GRAD_READY = BAR_DP_FULL + 2;      // [2] bf16 operands of the gradient MMAs written
+    static constexpr int BAR_DONE = BAR_GRAD_READY + 2;         // every MMA completed
     static constexpr int BAR_RES_TMEM = BAR_DONE + 1;           // resident tiles copied into TMEM
     static constexpr int NUM_BARS = BAR_RES_TMEM + 1;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;
-    static constexpr int NUM_THREADS = 192;   // 4 elementwise warps, producer, MMA
-    static constexpr int WARP_PRODUCER = 4;
-    static constexpr int WARP_MMA = 5;
+    static constexpr int NUM_THREADS = 32 * EW + 64;   // elementwise warps, producer, MMA
+    static constexpr int WARP_PRODUCER = EW;
+    static constexpr int WARP_MMA = EW + 1;
     static constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(RES, STR, false, false);
     static constexpr uint32_t IDESC_GRAD = ptx::idesc_bf16_f32(RES, D, false, true);
     static_assert(D == 64 || D == 128, "gradient kernels support D = 64 and 128");
     static_assert(RES == 128 && STR % 16 == 0 && STR >= 32 && STR <= 128, "tile shape");
+    static_assert(EW == 4 || EW == 8, "one or two elementwise warps per TMEM lane quarter");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
 };
 
@@ -213,6 +218,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 {
     using namespace ptx;
     static_assert(C::STR == BWD_STAT_ROWS, "one statistics tile per streamed query tile");
+    static_assert(C::EW == 8 && C::STR == 32, "two elementwise warps of 16 query columns per lane quarter");
     // K and V are also copied into TMEM (TM_KA, TM_VA) so that S^T = K Q^T and
     // dP^T = V dO^T read their A operand from TMEM instead of loading it from
     // shared memory for every instruction
@@ -247,11 +253,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_init(bar(C::BAR_STR_EMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(C::BAR_PAIR_FULL + b), 1);
-            mbar_init(bar(C::BAR_PAIR_READY + b), 4);   // one arrival per elementwise warp
+            mbar_init(bar(C::BAR_SCORE_FULL + b), 1);
+            mbar_init(bar(C::BAR_DP_FULL + b), 1);
+            mbar_init(bar(C::BAR_GRAD_READY + b), C::EW);   // one arrival per elementwise warp
         }
         mbar_init(bar(C::BAR_DONE), 1);
-        mbar_init(bar(C::BAR_RES_TMEM), 4);   // one arrival per elementwise warp
+        mbar_init(bar(C::BAR_RES_TMEM), C::EW);
         fence_mbar_init();
     }
     if (warp == C::WARP_MMA) {
@@ -329,6 +336,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             // K and V copied into TMEM by the elementwise warps
             ok = warp_wait_all(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
             tc_fence_after();
+            const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
             // S^T(b) = K Q^T and dP^T(b) = V dO^T for step s
             auto issue_pair = [&](int s) -> bool {
                 const int st = s % C::RING, b = s & 1;
@@ -337,36 +345,36 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     return false;
                 tc_fence_after();
                 if (leader) {
-                    const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < C::D / 16; ++kk) {
                         const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                        mma_ts(tmem + TM_ST + b * C::STR, tmem + TM_KA + kk * 8, desc_q + so + to, C::IDESC_PAIR,
-                               kk > 0 ? 1u : 0u);
-                        mma_ts(tmem + TM_DPT + b * C::STR, tmem + TM_VA + kk * 8, desc_do + so + to, C::IDESC_PAIR,
-                               kk > 0 ? 1u : 0u);
+                        mma_ts(tmem + TM_ST + b * C::STR, tmem + TM_KA + kk * 8, desc_q + stage_off(st) + to,
+                               C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                        mma_ts(tmem + TM_DPT + b * C::STR, tmem + TM_VA + kk * 8, desc_do + stage_off(st) + to,
+                               C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(bar(C::BAR_PAIR_FULL + b));
+                    mma_commit(bar(C::BAR_SCORE_FULL + b));
                 }
                 __syncwarp();
                 return true;
             };
-            // dV += P^T dO and dK += dS^T Q for step s
+            // dV += P^T dO and dK += dS^T Q for step s.  The bf16 pairs of query columns
+            // 16 kk .. 16 kk + 15 sit at column 16 kk of their buffer (8 columns), where
+            // the elementwise warp that owns those queries wrote them.
             auto issue_grad = [&](int s) -> bool {
                 const int st = s % C::RING, b = s & 1;
-                if (!warp_wait_all(bar(C::BAR_PAIR_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 3,
+                if (!warp_wait_all(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 3,
                                    p.wait_limit_ns))
                     return false;
                 tc_fence_after();
                 if (leader) {
-                    const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < C::STR / 16; ++kk) {
                         const uint64_t ko = static_cast<uint64_t>((kk * 16 * 128) >> 4);   // 16 rows
                         const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                        mma_ts(tmem + TM_DV, tmem + TM_ST + b * C::STR + kk * 8, desc_do_mn + so + ko,
+                        mma_ts(tmem + TM_DV, tmem + TM_ST + b * C::STR + kk * 16, desc_do_mn + stage_off(st) + ko,
                                C::IDESC_GRAD, acc);
-                        mma_ts(tmem + TM_DK, tmem + TM_DPT + b * C::STR + kk * 8, desc_q_mn + so + ko,
+                        mma_ts(tmem + TM_DK, tmem + TM_DPT + b * C::STR + kk * 16, desc_q_mn + stage_off(st) + ko,
                                C::IDESC_GRAD, acc);
                     }
                     mma_commit(bar(C::BAR_STR_EMPTY + st));   // this step's Q, dO and stats are free
@@ -390,17 +398,21 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
     } else {
         // ------------------------------------------------ elementwise warps
-        const int row = warp * 32 + lane;            // key row within the tile (TMEM lane)
+        // Two warps per 32-lane TMEM quarter: `half` 0 takes query columns 0..15 of
+        // every step (and copies K, stores dV), `half` 1 columns 16..31 (V, dK).
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;         // key row within the tile (TMEM lane)
         const int kj = k0 + row;                     // key index
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int c0 = 16 * half;                    // this warp's first query column of a step
         const float c2 = p.scale_log2;
         bool ok = true;
         if (n_steps > 0) {
-            // this row of K and of V into TMEM, as the score MMAs' A operands
+            // this row of K (half 0) or of V (half 1) into TMEM, as a score MMA's A operand
             ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
             if (ok) {
-                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_KA);
-                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES1, row, tmem + lane_base + TM_VA);
+                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + (half ? C::OFF_RES1 : C::OFF_RES0), row,
+                                                      tmem + lane_base + (half ? TM_VA : TM_KA));
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -410,7 +422,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         for (int s = 0; s < n_steps && ok; ++s) {
             const int st = s % C::RING, b = s & 1;
-            ok = warp_wait_all(bar(C::BAR_PAIR_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 1, p.wait_limit_ns);
+            ok = warp_wait_all(bar(C::BAR_SCORE_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 1, p.wait_limit_ns);
             if (!ok)
                 break;
             tc_fence_after();
@@ -421,91 +433,75 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                                p.wait_limit_ns);
             if (!ok)
                 break;
-            const uint32_t a_st = tmem + lane_base + TM_ST + b * C::STR;
-            const uint32_t a_dp = tmem + lane_base + TM_DPT + b * C::STR;
-            const uint32_t stat = sbase + C::OFF_STAT + st * 2 * C::STR * 4;
+            const uint32_t a_st = tmem + lane_base + TM_ST + b * C::STR + c0;
+            const uint32_t a_dp = tmem + lane_base + TM_DPT + b * C::STR + c0;
+            const uint32_t stat = sbase + C::OFF_STAT + st * C::STAT_BYTES;
             const int q0 = (qt0 + s) * C::STR;
             // query columns c < kj - q0 are masked (causal, key after query); only tiles
-            // reaching below some of this warp's keys need it
+            // whose first query of this half lies before this warp's last key need it
             const int first_visible = kj - q0;
-            const bool need_mask = p.causal && q0 < k0 + warp * 32 + 31;
+            const bool need_mask = p.causal && q0 + c0 < k0 + quarter * 32 + 31;
             const uint64_t c2x2 = f32x2(c2, c2);
             const uint64_t zero2 = 0;
-            uint32_t pw[C::STR / 2], dw[C::STR / 2];
+            uint32_t rs[16], rd[16], nl[16], nd[16];
+            tmem_ld16(a_st, rs);
+            tmem_ld16(a_dp, rd);
+            // -lse2 and -Delta of this warp's 16 queries (the same for every lane)
 #pragma unroll
-            for (int ch = 0; ch < C::STR / 32; ++ch) {
-                uint32_t rs[32], rd[32];
-                tmem_ld32(a_st + 32 * ch, rs);
-                tmem_ld32(a_dp + 32 * ch, rd);
-                // this chunk's -lse2 and -Delta (same for every lane: broadcast loads)
-                uint32_t nl[32], nd[32];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    ld_shared_v4(stat + (32 * ch + 4 * q) * 4, nl[4 * q], nl[4 * q + 1], nl[4 * q + 2], nl[4 * q + 3]);
-                    ld_shared_v4(stat + (C::STR + 32 * ch + 4 * q) * 4, nd[4 * q], nd[4 * q + 1], nd[4 * q + 2],
-                                 nd[4 * q + 3]);
-                }
-                tmem_ld_wait(rs);
-                tmem_ld_wait(rd);
-                float pv[32], dv[32];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float x0, x1;
-                    unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2x2,
-                                           f32x2(__uint_as_float(nl[e]), __uint_as_float(nl[e + 1]))),
-                                 x0, x1);
-                    pv[e] = ex2_approx(x0);
-                    pv[e + 1] = ex2_approx(x1);
-                    const uint64_t diff = add_f32x2(f32x2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])),
-                                                    f32x2(__uint_as_float(nd[e]), __uint_as_float(nd[e + 1])));
-                    unpack_f32x2(fma_f32x2(f32x2(pv[e], pv[e + 1]), diff, zero2), dv[e], dv[e + 1]);
-                }
-                if (need_mask) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (32 * ch + e < first_visible) {
-                            pv[e] = 0.f;
-                            dv[e] = 0.f;
-                        }
-                }
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    pw[(32 * ch + e) / 2] = bwd_pack(pv[e], pv[e + 1]);
-                    dw[(32 * ch + e) / 2] = bwd_pack(dv[e], dv[e + 1]);
-                }
+            for (int q = 0; q < 4; ++q) {
+                ld_shared_v4(stat + (c0 + 4 * q) * 4, nl[4 * q], nl[4 * q + 1], nl[4 * q + 2], nl[4 * q + 3]);
+                ld_shared_v4(stat + (C::STR + c0 + 4 * q) * 4, nd[4 * q], nd[4 * q + 1], nd[4 * q + 2],
+                             nd[4 * q + 3]);
             }
-            // P^T and dS^T as bf16 pairs over the first STR/2 columns of their buffers
-            if constexpr (C::STR / 2 >= 32) {
+            tmem_ld_wait(rs, rd);
+            float pv[16], dv[16];
 #pragma unroll
-                for (int q = 0; q < C::STR / 64; ++q) {
-                    tmem_st32(a_st + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pw + 32 * q));
-                    tmem_st32(a_dp + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(dw + 32 * q));
-                }
-            } else {
-                tmem_st16(a_st, pw);
-                tmem_st16(a_dp, dw);
+            for (int e = 0; e < 16; e += 2) {
+                float x0, x1;
+                unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2x2,
+                                       f32x2(__uint_as_float(nl[e]), __uint_as_float(nl[e + 1]))),
+                             x0, x1);
+                pv[e] = ex2_approx(x0);
+                pv[e + 1] = ex2_approx(x1);
+                const uint64_t diff = add_f32x2(f32x2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])),
+                                                f32x2(__uint_as_float(nd[e]), __uint_as_float(nd[e + 1])));
+                unpack_f32x2(fma_f32x2(f32x2(pv[e], pv[e + 1]), diff, zero2), dv[e], dv[e + 1]);
             }
+            if (need_mask) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (c0 + e < first_visible) {
+                        pv[e] = 0.f;
+                        dv[e] = 0.f;
+                    }
+            }
+            // P^T and dS^T as bf16 pairs over the first 8 of this warp's 16 columns
+            uint32_t pw[8], dw[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                pw[e / 2] = bwd_pack(pv[e], pv[e + 1]);
+                dw[e / 2] = bwd_pack(dv[e], dv[e + 1]);
+            }
+            tmem_st8(a_st, pw);
+            tmem_st8(a_dp, dw);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar(C::BAR_PAIR_READY + b));
+                mbar_arrive(bar(C::BAR_GRAD_READY + b));
         }
-        // epilogue: dV and scale * dK rows (zeros when no query sees these keys)
+        // epilogue: dV (half 0) or scale * dK (half 1) rows; zeros when no query sees
+        // these keys
         const bool valid = kj < p.Lk;
-        uint16_t *dv_row = p.dv + (static_cast<size_t>(bh) * p.Lk + (valid ? kj : 0)) * C::D;
-        uint16_t *dk_row = p.dk + (static_cast<size_t>(bh) * p.Lk + (valid ? kj : 0)) * C::D;
+        uint16_t *out_row = (half ? p.dk : p.dv) + (static_cast<size_t>(bh) * p.Lk + (valid ? kj : 0)) * C::D;
         if (n_steps == 0) {
             if (valid) {
-                for (int d = 0; d < C::D; d += 8) {
-                    *reinterpret_cast<uint4 *>(dv_row + d) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(dk_row + d) = make_uint4(0, 0, 0, 0);
-                }
+                for (int d = 0; d < C::D; d += 8)
+                    *reinterpret_cast<uint4 *>(out_row + d) = make_uint4(0, 0, 0, 0);
             }
         } else if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 2, p.wait_limit_ns)) {
             tc_fence_after();
-            store_acc_row<C::D>(tmem + lane_base + TM_DV, 1.f, dv_row, valid);
-            store_acc_row<C::D>(tmem + lane_base + TM_DK, p.scale, dk_row, valid);
+            store_acc_row<C::D>(tmem + lane_base + (half ? TM_DK : TM_DV), half ? p.scale : 1.f, out_row, valid);
         }
     }
 
@@ -528,6 +524,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                      const BwdParams p)
 {
     using namespace ptx;
+    static_assert(C::EW == 4, "one elementwise warp per lane quarter");
     // Q and dO are also copied into TMEM (TM_QA, TM_DOA) so that S = Q K^T and
     // dP = dO V^T read their A operand from TMEM instead of loading it from shared
     // memory for every instruction
@@ -561,11 +558,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_init(bar(C::BAR_STR_EMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(C::BAR_PAIR_FULL + b), 1);
-            mbar_init(bar(C::BAR_PAIR_READY + b), 4);
+            mbar_init(bar(C::BAR_SCORE_FULL + b), 1);
+            mbar_init(bar(C::BAR_DP_FULL + b), 1);
+            mbar_init(bar(C::BAR_GRAD_READY + b), C::EW);   // one arrival per elementwise warp
         }
         mbar_init(bar(C::BAR_DONE), 1);
-        mbar_init(bar(C::BAR_RES_TMEM), 4);   // one arrival per elementwise warp
+        mbar_init(bar(C::BAR_RES_TMEM), C::EW);
         fence_mbar_init();
     }
     if (warp == C::WARP_MMA) {
@@ -624,54 +622,73 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         // Q and dO copied into TMEM by the elementwise warps
         bool ok = warp_wait_all(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
         tc_fence_after();
-        // S(b) = Q K^T and dP(b) = dO V^T for step s
-        auto issue_pair = [&](int s) -> bool {
+        const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
+        // S(b) = Q K^T for step s, once the step's tiles have landed
+        auto issue_s = [&](int s) -> bool {
             const int st = s % C::RING, b = s & 1;
             if (!warp_wait_all(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_MMA | 6,
                                p.wait_limit_ns))
                 return false;
             tc_fence_after();
             if (leader) {
-                const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::D / 16; ++kk) {
                     const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                    mma_ts(tmem + TM_S + b * C::STR, tmem + TM_QA + kk * 8, desc_k + so + to, C::IDESC_PAIR,
-                           kk > 0 ? 1u : 0u);
-                    mma_ts(tmem + TM_DP + b * C::STR, tmem + TM_DOA + kk * 8, desc_v + so + to, C::IDESC_PAIR,
-                           kk > 0 ? 1u : 0u);
+                    mma_ts(tmem + TM_S + b * C::STR, tmem + TM_QA + kk * 8, desc_k + stage_off(st) + to,
+                           C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(C::BAR_PAIR_FULL + b));
+                mma_commit(bar(C::BAR_SCORE_FULL + b));
             }
             __syncwarp();
             return true;
         };
+        // dP(b) = dO V^T for step s (issued after issue_s(s), which waited for the tiles)
+        auto issue_dp = [&](int s) {
+            const int st = s % C::RING, b = s & 1;
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < C::D / 16; ++kk) {
+                    const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
+                    mma_ts(tmem + TM_DP + b * C::STR, tmem + TM_DOA + kk * 8, desc_v + stage_off(st) + to,
+                           C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(C::BAR_DP_FULL + b));
+            }
+            __syncwarp();
+        };
         // dQ += dS K for step s
         auto issue_grad = [&](int s) -> bool {
             const int st = s % C::RING, b = s & 1;
-            if (!warp_wait_all(bar(C::BAR_PAIR_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 7, p.wait_limit_ns))
+            if (!warp_wait_all(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 7, p.wait_limit_ns))
                 return false;
             tc_fence_after();
             if (leader) {
-                const uint64_t so = static_cast<uint64_t>((st * C::STR_TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < C::STR / 16; ++kk)
                     mma_ts(tmem + TM_DQ, tmem + TM_S + b * C::STR + kk * 8,
-                           desc_k_mn + so + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_GRAD,
+                           desc_k_mn + stage_off(st) + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_GRAD,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(C::BAR_STR_EMPTY + st));
             }
             __syncwarp();
             return true;
         };
+        // S and dP are committed separately so that the elementwise warps start on
+        // the exponentials while dP is still being computed
         if (ok)
-            ok = issue_pair(0);
+            ok = issue_s(0);
+        if (ok)
+            issue_dp(0);
         if (ok && n_steps > 1)
-            ok = issue_pair(1);
+            ok = issue_s(1);
+        if (ok && n_steps > 1)
+            issue_dp(1);
         for (int s = 0; s < n_steps && ok; ++s) {
             ok = issue_grad(s);
             if (ok && s + 2 < n_steps)
-                ok = issue_pair(s + 2);
+                ok = issue_s(s + 2);
+            if (ok && s + 2 < n_steps)
+                issue_dp(s + 2);
         }
         if (leader)
             mma_commit(bar(C::BAR_DONE));
@@ -704,7 +721,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         for (int s = 0; s < n_steps && ok; ++s) {
             const int b = s & 1;
-            ok = warp_wait_all(bar(C::BAR_PAIR_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 3, p.wait_limit_ns);
+            ok = warp_wait_all(bar(C::BAR_SCORE_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 3, p.wait_limit_ns);
             if (!ok)
                 break;
             tc_fence_after();
@@ -718,23 +735,39 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const uint64_t nl2 = f32x2(-lse2, -lse2);
             const uint64_t nd2 = f32x2(-dl, -dl);
             const uint64_t zero2 = 0;
-            uint32_t dw[C::STR / 2];
+            // P = 2^(S c - lse2) for the whole tile, before dP is needed
+            float pv[C::STR];
 #pragma unroll
             for (int ch = 0; ch < C::STR / 32; ++ch) {
-                uint32_t rs[32], rd[32];
+                uint32_t rs[32];
                 tmem_ld32(a_s + 32 * ch, rs);
-                tmem_ld32(a_dp + 32 * ch, rd);
                 tmem_ld_wait(rs);
-                tmem_ld_wait(rd);
-                float dv[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float x0, x1;
                     unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2x2, nl2), x0,
                                  x1);
-                    const uint64_t pp = f32x2(ex2_approx(x0), ex2_approx(x1));
+                    pv[32 * ch + e] = ex2_approx(x0);
+                    pv[32 * ch + e + 1] = ex2_approx(x1);
+                }
+            }
+            // dS = P (dP - Delta), once dP is in
+            ok = warp_wait_all(bar(C::BAR_DP_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 9, p.wait_limit_ns);
+            if (!ok)
+                break;
+            tc_fence_after();
+            uint32_t dw[C::STR / 2];
+#pragma unroll
+            for (int ch = 0; ch < C::STR / 32; ++ch) {
+                uint32_t rd[32];
+                tmem_ld32(a_dp + 32 * ch, rd);
+                tmem_ld_wait(rd);
+                float dv[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
                     const uint64_t diff = add_f32x2(f32x2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])), nd2);
-                    unpack_f32x2(fma_f32x2(pp, diff, zero2), dv[e], dv[e + 1]);
+                    unpack_f32x2(fma_f32x2(f32x2(pv[32 * ch + e], pv[32 * ch + e + 1]), diff, zero2), dv[e],
+                                 dv[e + 1]);
                 }
                 if (need_mask) {
 #pragma unroll
@@ -746,6 +779,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 for (int e = 0; e < 32; e += 2)
                     dw[(32 * ch + e) / 2] = bwd_pack(dv[e], dv[e + 1]);
             }
+            // dS as bf16 pairs over the first STR/2 columns of the S buffer
             if constexpr (C::STR / 2 >= 32) {
 #pragma unroll
                 for (int q = 0; q < C::STR / 64; ++q)
@@ -757,7 +791,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar(C::BAR_PAIR_READY + b));
+                mbar_arrive(bar(C::BAR_GRAD_READY + b));
         }
         if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 4, p.wait_limit_ns)) {
             tc_fence_after();
