@@ -443,163 +443,163 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         __syncwarp();
       } else if (warp == C::WARP_MMA) {
         // ================================================== MMA issuer
-        // The whole warp runs the (uniform) control flow and the waits; one
-        // elected lane issues the MMAs and commits.
-        const bool leader = elect_one();
-        // Descriptor bases; a K step moves the start address, which is the low
-        // field of the descriptor in 16-byte units, so it is a plain add.
-        const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-        const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-        const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_V, C::KV_BLOCK, 1024);
-        uint32_t kv_iter = 0;              // ring position of the current unit's K/V tile 0
-        uint32_t tbase[C::NQ] = {};        // S/PV tiles of each Q buffer in earlier units
-        uint32_t q_loads[C::NQ] = {};      // Q loads consumed per Q buffer
-        uint32_t units[C::NQ] = {};        // earlier units that used each Q buffer
-        bool ok = true;
+        // One elected lane runs the whole issue loop -- its waits, MMAs and
+        // commits -- and the other lanes wait at the final __syncwarp.  (MMAs
+        // issued from a branch that the rest of the warp skips, once per group,
+        // cost 20-40 clk more each than back-to-back issue from one thread.)
+        if (elect_one()) {
+            // Descriptor bases; a K step moves the start address, which is the low
+            // field of the descriptor in 16-byte units, so it is a plain add.
+            const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+            const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+            const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_V, C::KV_BLOCK, 1024);
+            uint32_t kv_iter = 0;              // ring position of the current unit's K/V tile 0
+            uint32_t tbase[C::NQ] = {};        // S/PV tiles of each Q buffer in earlier units
+            uint32_t q_loads[C::NQ] = {};      // Q loads consumed per Q buffer
+            uint32_t units[C::NQ] = {};        // earlier units that used each Q buffer
+            bool ok = true;
 
-        for (int i = 0; ok; ++i) {
-            Segment sg;
-            if (!segment_at(i, p, ranges, sg))
-                break;
-            int qg, bh;
-            decode_unit(sg.unit, p, qg, bh);
-            const int q0 = qg * (C::NQ * C::BM);
-            int n_t[C::NQ];
-            int n_max = 0;
-#pragma unroll
-            for (int t = 0; t < C::NQ; ++t) {
-                n_t[t] = segment_tiles(sg, q0 + t * C::BM, p, C::BN);
-                n_max = max(n_max, n_t[t]);
-            }
-            // QT: the TMEM buffer holding this segment's Q (segments alternate)
-            const uint32_t qt_buf = q_loads[0] % C::QB;
-            // the last Q tile (highest t) that reads K/V tile j
-            auto last_user = [&](int j) {
-                int lu = 0;
-#pragma unroll
-                for (int t = 0; t < C::NQ; ++t)
-                    if (j < n_t[t])
-                        lu = t;
-                return lu;
-            };
-
-            // S(t, j) = Q_t K_j^T  into S/P buffer (t, (tbase + j) % NS)
-            auto issue_s = [&](int t, int j) -> bool {
-                const uint32_t it = kv_iter + j;
-                const int s = it % C::KS;
-                if (!warp_wait(bar(C::BAR_K_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 2, p.wait_limit_ns))
-                    return false;
-                tc_fence_after();
-                const uint32_t g = tbase[t] + j;
-                const int b = g % C::NS;
-                if (leader) {
-                    const uint32_t d = tmem + C::TM_S + (t * C::NS + b) * C::BN;
-                    const uint64_t dk = desc_k + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
-                    if constexpr (C::QT) {
-                        // A = Q from TMEM buffer qt_buf: 16 bf16 (8 columns) per K step
-                        const uint32_t a = tmem + C::TM_Q + qt_buf * (C::D / 2);
-#pragma unroll
-                        for (int kk = 0; kk < C::D / 16; ++kk)
-                            mma_ts(d, a + kk * 8,
-                                   dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
-                                   C::IDESC_S, kk > 0 ? 1u : 0u);
-                    } else {
-                        const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < C::D / 16; ++kk)
-                            mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
-                                   dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
-                                   C::IDESC_S, kk > 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(C::BAR_S_FULL + t * C::NS + b));
-                    if (last_user(j) == t)
-                        mma_commit(bar(C::BAR_K_EMPTY + s));
-                    if (j == n_t[t] - 1)   // last read of this unit's Q tile
-                        mma_commit(bar(C::QT ? C::BAR_QT_EMPTY + qt_buf : C::BAR_Q_EMPTY + t));
-                }
-                __syncwarp();
-                return true;
-            };
-            // O_t (+)= P(t, j) V_j, P read from TMEM
-            auto issue_pv = [&](int t, int j) -> bool {
-                const uint32_t it = kv_iter + j;
-                const int s = it % C::KS;
-                const uint32_t g = tbase[t] + j;
-                const int b = g % C::NS;
-                if (!warp_wait(bar(C::BAR_P_READY + t * C::NS + b), (g / C::NS) & 1, p.err, ERR_MMA | 3,
-                               p.wait_limit_ns))
-                    return false;
-                if (!warp_wait(bar(C::BAR_V_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
-                    return false;
-                // the first PV of a unit overwrites O_t: the previous unit's epilogue
-                // must have read it out of TMEM
-                if (j == 0 && units[t] > 0 &&
-                    !warp_wait(bar(C::BAR_O_FREE + t), (units[t] - 1) & 1, p.err, ERR_MMA | 5, p.wait_limit_ns))
-                    return false;
-                tc_fence_after();
-                if (leader) {
-                    const uint32_t d = tmem + C::TM_O + t * C::D;
-                    const uint32_t a = tmem + C::TM_S + (t * C::NS + b) * C::BN;
-                    const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
-#pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; ++kk)
-                        mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(bar(C::BAR_O_DONE + t));
-                    if (last_user(j) == t)
-                        mma_commit(bar(C::BAR_V_EMPTY + s));
-                }
-                __syncwarp();
-                return true;
-            };
-
-            // this unit's Q tiles: in shared memory (TMA), or copied into TMEM buffer
-            // qt_buf by the softmax warps
-#pragma unroll
-            for (int t = 0; t < C::NQ; ++t) {
-                if (ok && n_t[t] > 0) {
-                    if constexpr (C::QT)
-                        ok = warp_wait(bar(C::BAR_QT_FULL + qt_buf), (q_loads[0] / C::QB) & 1, p.err,
-                                       ERR_MMA | 6, p.wait_limit_ns);
-                    else
-                        ok = warp_wait(bar(C::BAR_Q_FULL + t), q_loads[t] & 1, p.err, ERR_MMA | 1,
-                                       p.wait_limit_ns);
-                    ++q_loads[t];
-                }
-            }
-            // Issue order: S for the first NS tiles of every Q tile, then per K/V
-            // tile j and Q tile t: PV(t, j) followed by S(t, j + NS), which reuses
-            // the TMEM buffer PV(t, j) just read (tcgen05 ops execute in order).
-#pragma unroll
-            for (int b = 0; b < C::NS; ++b)
-#pragma unroll
-                for (int t = 0; t < C::NQ; ++t)
-                    if (ok && b < n_t[t])
-                        ok = issue_s(t, b);
-            for (int j = 0; j < n_max && ok; ++j) {
-#pragma unroll
+            for (int i = 0; ok; ++i) {
+                Segment sg;
+                if (!segment_at(i, p, ranges, sg))
+                    break;
+                int qg, bh;
+                decode_unit(sg.unit, p, qg, bh);
+                const int q0 = qg * (C::NQ * C::BM);
+                int n_t[C::NQ];
+                int n_max = 0;
+    #pragma unroll
                 for (int t = 0; t < C::NQ; ++t) {
-                    if (ok && j < n_t[t]) {
-                        ok = issue_pv(t, j);
-                        if (ok && j + C::NS < n_t[t])
-                            ok = issue_s(t, j + C::NS);
+                    n_t[t] = segment_tiles(sg, q0 + t * C::BM, p, C::BN);
+                    n_max = max(n_max, n_t[t]);
+                }
+                // QT: the TMEM buffer holding this segment's Q (segments alternate)
+                const uint32_t qt_buf = q_loads[0] % C::QB;
+                // the last Q tile (highest t) that reads K/V tile j
+                auto last_user = [&](int j) {
+                    int lu = 0;
+    #pragma unroll
+                    for (int t = 0; t < C::NQ; ++t)
+                        if (j < n_t[t])
+                            lu = t;
+                    return lu;
+                };
+
+                // S(t, j) = Q_t K_j^T  into S/P buffer (t, (tbase + j) % NS)
+                auto issue_s = [&](int t, int j) -> bool {
+                    const uint32_t it = kv_iter + j;
+                    const int s = it % C::KS;
+                    if (!lone_wait(bar(C::BAR_K_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 2, p.wait_limit_ns))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t g = tbase[t] + j;
+                    const int b = g % C::NS;
+                    {
+                        const uint32_t d = tmem + C::TM_S + (t * C::NS + b) * C::BN;
+                        const uint64_t dk = desc_k + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
+                        if constexpr (C::QT) {
+                            // A = Q from TMEM buffer qt_buf: 16 bf16 (8 columns) per K step
+                            const uint32_t a = tmem + C::TM_Q + qt_buf * (C::D / 2);
+    #pragma unroll
+                            for (int kk = 0; kk < C::D / 16; ++kk)
+                                mma_ts(d, a + kk * 8,
+                                       dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
+                                       C::IDESC_S, kk > 0 ? 1u : 0u);
+                        } else {
+                            const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
+    #pragma unroll
+                            for (int kk = 0; kk < C::D / 16; ++kk)
+                                mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
+                                       dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
+                                       C::IDESC_S, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(C::BAR_S_FULL + t * C::NS + b));
+                        if (last_user(j) == t)
+                            mma_commit(bar(C::BAR_K_EMPTY + s));
+                        if (j == n_t[t] - 1)   // last read of this unit's Q tile
+                            mma_commit(bar(C::QT ? C::BAR_QT_EMPTY + qt_buf : C::BAR_Q_EMPTY + t));
+                    }
+                    return true;
+                };
+                // O_t (+)= P(t, j) V_j, P read from TMEM
+                auto issue_pv = [&](int t, int j) -> bool {
+                    const uint32_t it = kv_iter + j;
+                    const int s = it % C::KS;
+                    const uint32_t g = tbase[t] + j;
+                    const int b = g % C::NS;
+                    if (!lone_wait(bar(C::BAR_P_READY + t * C::NS + b), (g / C::NS) & 1, p.err, ERR_MMA | 3,
+                                   p.wait_limit_ns))
+                        return false;
+                    if (!lone_wait(bar(C::BAR_V_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
+                        return false;
+                    // the first PV of a unit overwrites O_t: the previous unit's epilogue
+                    // must have read it out of TMEM
+                    if (j == 0 && units[t] > 0 &&
+                        !lone_wait(bar(C::BAR_O_FREE + t), (units[t] - 1) & 1, p.err, ERR_MMA | 5, p.wait_limit_ns))
+                        return false;
+                    tc_fence_after();
+                    {
+                        const uint32_t d = tmem + C::TM_O + t * C::D;
+                        const uint32_t a = tmem + C::TM_S + (t * C::NS + b) * C::BN;
+                        const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
+    #pragma unroll
+                        for (int kk = 0; kk < C::BN / 16; ++kk)
+                            mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(bar(C::BAR_O_DONE + t));
+                        if (last_user(j) == t)
+                            mma_commit(bar(C::BAR_V_EMPTY + s));
+                    }
+                    return true;
+                };
+
+                // this unit's Q tiles: in shared memory (TMA), or copied into TMEM buffer
+                // qt_buf by the softmax warps
+    #pragma unroll
+                for (int t = 0; t < C::NQ; ++t) {
+                    if (ok && n_t[t] > 0) {
+                        if constexpr (C::QT)
+                            ok = lone_wait(bar(C::BAR_QT_FULL + qt_buf), (q_loads[0] / C::QB) & 1, p.err,
+                                           ERR_MMA | 6, p.wait_limit_ns);
+                        else
+                            ok = lone_wait(bar(C::BAR_Q_FULL + t), q_loads[t] & 1, p.err, ERR_MMA | 1,
+                                           p.wait_limit_ns);
+                        ++q_loads[t];
                     }
                 }
-            }
-#pragma unroll
-            for (int t = 0; t < C::NQ; ++t) {
-                if (n_t[t] > 0) {
-                    tbase[t] += n_t[t];
-                    ++units[t];
+                // Issue order: S for the first NS tiles of every Q tile, then per K/V
+                // tile j and Q tile t: PV(t, j) followed by S(t, j + NS), which reuses
+                // the TMEM buffer PV(t, j) just read (tcgen05 ops execute in order).
+    #pragma unroll
+                for (int b = 0; b < C::NS; ++b)
+    #pragma unroll
+                    for (int t = 0; t < C::NQ; ++t)
+                        if (ok && b < n_t[t])
+                            ok = issue_s(t, b);
+                for (int j = 0; j < n_max && ok; ++j) {
+    #pragma unroll
+                    for (int t = 0; t < C::NQ; ++t) {
+                        if (ok && j < n_t[t]) {
+                            ok = issue_pv(t, j);
+                            if (ok && j + C::NS < n_t[t])
+                                ok = issue_s(t, j + C::NS);
+                        }
+                    }
                 }
+    #pragma unroll
+                for (int t = 0; t < C::NQ; ++t) {
+                    if (n_t[t] > 0) {
+                        tbase[t] += n_t[t];
+                        ++units[t];
+                    }
+                }
+                kv_iter += n_max;
             }
-            kv_iter += n_max;
-        }
-        // drain: every MMA issued above has completed before TMEM can be released
-        if (leader)
+            // drain: every MMA issued above has completed before TMEM can be released
             mma_commit(bar(C::BAR_DRAIN));
+            lone_wait(bar(C::BAR_DRAIN), 0, p.err, ERR_DRAIN | 4, p.wait_limit_ns);
+        }
         __syncwarp();
-        warp_wait(bar(C::BAR_DRAIN), 0, p.err, ERR_DRAIN | 4, p.wait_limit_ns);
       }
     } else {
         // ================================================== softmax warps

@@ -108,6 +108,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *er
     }
 }
 
+// Bounded wait by a thread whose warp-mates are not waiting with it (a lane
+// running a loop of its own).  It polls with test_wait, which never suspends: a
+// lone lane suspended in try_wait was seen to miss the phase completion.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool lone_wait(uint32_t bar, uint32_t parity, int *err, int code, uint64_t limit_ns)
+{
+    if (mbar_test_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_test_wait(bar, parity))
+                return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicCAS(err, 0, code);
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap)
 {
