@@ -323,28 +323,29 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == C::WARP_MMA) {
-        // ------------------------------------------------ MMA issuer (elected lane)
-        const bool leader = elect_one();
-        bool ok = true;
-        if (n_steps > 0) {
-            const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
-            const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
-            // the same streamed tiles as MN-major B operands (N = D along the rows'
-            // 128-byte lines, K = query rows)
-            const uint64_t desc_q_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
-            const uint64_t desc_do_mn = sdesc_sw128(sbase + C::OFF_STR1, C::STR_BLOCK, 1024);
-            // K and V copied into TMEM by the elementwise warps
-            ok = warp_wait_all(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
-            tc_fence_after();
-            const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
-            // S^T(b) = K Q^T and dP^T(b) = V dO^T for step s
-            auto issue_pair = [&](int s) -> bool {
-                const int st = s % C::RING, b = s & 1;
-                if (!warp_wait_all(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_MMA | 2,
-                                   p.wait_limit_ns))
-                    return false;
+        // ------------------------------------------------ MMA issuer
+        // One elected lane runs the whole issue loop (waits, MMAs, commits); the
+        // rest of the warp waits at the final __syncwarp.
+        if (elect_one()) {
+            bool ok = true;
+            if (n_steps > 0) {
+                const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
+                const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
+                // the same streamed tiles as MN-major B operands (N = D along the rows'
+                // 128-byte lines, K = query rows)
+                const uint64_t desc_q_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
+                const uint64_t desc_do_mn = sdesc_sw128(sbase + C::OFF_STR1, C::STR_BLOCK, 1024);
+                // K and V copied into TMEM by the elementwise warps
+                ok = lone_wait(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
                 tc_fence_after();
-                if (leader) {
+                const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
+                // S^T(b) = K Q^T and dP^T(b) = V dO^T for step s
+                auto issue_pair = [&](int s) -> bool {
+                    const int st = s % C::RING, b = s & 1;
+                    if (!lone_wait(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_MMA | 2,
+                                   p.wait_limit_ns))
+                        return false;
+                    tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < C::D / 16; ++kk) {
                         const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
@@ -354,20 +355,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                                C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(C::BAR_SCORE_FULL + b));
-                }
-                __syncwarp();
-                return true;
-            };
-            // dV += P^T dO and dK += dS^T Q for step s.  The bf16 pairs of query columns
-            // 16 kk .. 16 kk + 15 sit at column 16 kk of their buffer (8 columns), where
-            // the elementwise warp that owns those queries wrote them.
-            auto issue_grad = [&](int s) -> bool {
-                const int st = s % C::RING, b = s & 1;
-                if (!warp_wait_all(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 3,
+                    return true;
+                };
+                // dV += P^T dO and dK += dS^T Q for step s.  The bf16 pairs of query columns
+                // 16 kk .. 16 kk + 15 sit at column 16 kk of their buffer (8 columns), where
+                // the elementwise warp that owns those queries wrote them.
+                auto issue_grad = [&](int s) -> bool {
+                    const int st = s % C::RING, b = s & 1;
+                    if (!lone_wait(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 3,
                                    p.wait_limit_ns))
-                    return false;
-                tc_fence_after();
-                if (leader) {
+                        return false;
+                    tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < C::STR / 16; ++kk) {
                         const uint64_t ko = static_cast<uint64_t>((kk * 16 * 128) >> 4);   // 16 rows
@@ -378,24 +376,22 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                                C::IDESC_GRAD, acc);
                     }
                     mma_commit(bar(C::BAR_STR_EMPTY + st));   // this step's Q, dO and stats are free
+                    return true;
+                };
+                if (ok)
+                    ok = issue_pair(0);
+                if (ok && n_steps > 1)
+                    ok = issue_pair(1);
+                for (int s = 0; s < n_steps && ok; ++s) {
+                    ok = issue_grad(s);
+                    if (ok && s + 2 < n_steps)
+                        ok = issue_pair(s + 2);   // into the buffers issue_grad(s) just read
                 }
-                __syncwarp();
-                return true;
-            };
-            if (ok)
-                ok = issue_pair(0);
-            if (ok && n_steps > 1)
-                ok = issue_pair(1);
-            for (int s = 0; s < n_steps && ok; ++s) {
-                ok = issue_grad(s);
-                if (ok && s + 2 < n_steps)
-                    ok = issue_pair(s + 2);   // into the buffers issue_grad(s) just read
-            }
-            if (leader)
                 mma_commit(bar(C::BAR_DONE));
-            __syncwarp();
-            warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 4, p.wait_limit_ns);
+                lone_wait(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 4, p.wait_limit_ns);
+            }
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------ elementwise warps
         // Two warps per 32-lane TMEM quarter: `half` 0 takes query columns 0..15 of
@@ -615,22 +611,22 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == C::WARP_MMA) {
-        const bool leader = elect_one();
-        const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
-        const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
-        const uint64_t desc_k_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
-        // Q and dO copied into TMEM by the elementwise warps
-        bool ok = warp_wait_all(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
-        tc_fence_after();
-        const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
-        // S(b) = Q K^T for step s, once the step's tiles have landed
-        auto issue_s = [&](int s) -> bool {
-            const int st = s % C::RING, b = s & 1;
-            if (!warp_wait_all(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_MMA | 6,
-                               p.wait_limit_ns))
-                return false;
+        // one elected lane runs the whole issue loop (waits, MMAs, commits)
+        if (elect_one()) {
+            const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
+            const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
+            const uint64_t desc_k_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
+            // Q and dO copied into TMEM by the elementwise warps
+            bool ok = lone_wait(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
             tc_fence_after();
-            if (leader) {
+            const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
+            // S(b) = Q K^T for step s, once the step's tiles have landed
+            auto issue_s = [&](int s) -> bool {
+                const int st = s % C::RING, b = s & 1;
+                if (!lone_wait(bar(C::BAR_STR_FULL + st), (s / C::RING) & 1, p.err, ERR_BWD_MMA | 6,
+                               p.wait_limit_ns))
+                    return false;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C::D / 16; ++kk) {
                     const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
@@ -638,14 +634,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                            C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::BAR_SCORE_FULL + b));
-            }
-            __syncwarp();
-            return true;
-        };
-        // dP(b) = dO V^T for step s (issued after issue_s(s), which waited for the tiles)
-        auto issue_dp = [&](int s) {
-            const int st = s % C::RING, b = s & 1;
-            if (leader) {
+                return true;
+            };
+            // dP(b) = dO V^T for step s (issued after issue_s(s), which waited for the tiles)
+            auto issue_dp = [&](int s) {
+                const int st = s % C::RING, b = s & 1;
 #pragma unroll
                 for (int kk = 0; kk < C::D / 16; ++kk) {
                     const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
@@ -653,47 +646,42 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                            C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::BAR_DP_FULL + b));
-            }
-            __syncwarp();
-        };
-        // dQ += dS K for step s
-        auto issue_grad = [&](int s) -> bool {
-            const int st = s % C::RING, b = s & 1;
-            if (!warp_wait_all(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 7, p.wait_limit_ns))
-                return false;
-            tc_fence_after();
-            if (leader) {
+            };
+            // dQ += dS K for step s
+            auto issue_grad = [&](int s) -> bool {
+                const int st = s % C::RING, b = s & 1;
+                if (!lone_wait(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 7, p.wait_limit_ns))
+                    return false;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C::STR / 16; ++kk)
                     mma_ts(tmem + TM_DQ, tmem + TM_S + b * C::STR + kk * 8,
                            desc_k_mn + stage_off(st) + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_GRAD,
                            (s > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(C::BAR_STR_EMPTY + st));
+                return true;
+            };
+            // S and dP are committed separately so that the elementwise warps start on
+            // the exponentials while dP is still being computed
+            if (ok)
+                ok = issue_s(0);
+            if (ok)
+                issue_dp(0);
+            if (ok && n_steps > 1)
+                ok = issue_s(1);
+            if (ok && n_steps > 1)
+                issue_dp(1);
+            for (int s = 0; s < n_steps && ok; ++s) {
+                ok = issue_grad(s);
+                if (ok && s + 2 < n_steps)
+                    ok = issue_s(s + 2);
+                if (ok && s + 2 < n_steps)
+                    issue_dp(s + 2);
             }
-            __syncwarp();
-            return true;
-        };
-        // S and dP are committed separately so that the elementwise warps start on
-        // the exponentials while dP is still being computed
-        if (ok)
-            ok = issue_s(0);
-        if (ok)
-            issue_dp(0);
-        if (ok && n_steps > 1)
-            ok = issue_s(1);
-        if (ok && n_steps > 1)
-            issue_dp(1);
-        for (int s = 0; s < n_steps && ok; ++s) {
-            ok = issue_grad(s);
-            if (ok && s + 2 < n_steps)
-                ok = issue_s(s + 2);
-            if (ok && s + 2 < n_steps)
-                issue_dp(s + 2);
-        }
-        if (leader)
             mma_commit(bar(C::BAR_DONE));
+            lone_wait(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 8, p.wait_limit_ns);
+        }
         __syncwarp();
-        warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 8, p.wait_limit_ns);
     } else {
         const int row = warp * 32 + lane;            // query row within the tile
         const int qi = q0 + row;
