@@ -5,6 +5,7 @@
 
 #include <atomic>
 #include <climits>
+#include <mutex>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -57,11 +58,51 @@ inline WorkspaceLayout workspace_layout(long long G, int NQ, int D)
 
 enum SplitPolicy { SPLIT_NEVER = 0, SPLIT_AUTO = 1, SPLIT_ALWAYS = 2 };
 
+// A cut of the non-causal iterations into cost-balanced ranges (cut_ranges).  The
+// cut is a pure function of (units, n_kv, G) but costs a binary search over greedy
+// passes -- tens of microseconds of host time -- so the last few are kept and
+// repeated launches of one shape reuse theirs.
+struct SplitPlan {
+    long long units = -1, n_kv = -1;
+    int G = 0;
+    int k = 0;        // ranges
+    long long T = 0;  // largest range cost
+    int begin[MAX_SPLIT_CTAS + 1];
+};
+
+inline SplitPlan split_plan(long long units, long long n_kv, int G)
+{
+    constexpr int SLOTS = 4;
+    static std::mutex mu;
+    static SplitPlan cache[SLOTS];
+    static int next = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const SplitPlan &c : cache)
+            if (c.units == units && c.n_kv == n_kv && c.G == G)
+                return c;
+    }
+    SplitPlan plan;
+    plan.units = units;
+    plan.n_kv = n_kv;
+    plan.G = G;
+    plan.k = cut_ranges(units, n_kv, G, plan.begin, &plan.T);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[next] = plan;
+    next = (next + 1) % SLOTS;
+    return plan;
+}
+
 inline bool use_split(int policy, long long units, long long n_kv, int num_sms)
 {
     if (units * n_kv > INT_MAX)
         return false;
-    return policy == SPLIT_ALWAYS || (policy == SPLIT_AUTO && split_pays(units, n_kv, num_sms));
+    if (policy == SPLIT_ALWAYS)
+        return true;
+    if (policy != SPLIT_AUTO)
+        return false;
+    const SplitPlan plan = split_plan(units, n_kv, static_cast<int>(split_grid(units, n_kv, num_sms)));
+    return split_pays_given(units, n_kv, num_sms, plan.T);
 }
 
 // Bytes of workspace the pass needs for its split schedule (0: none is used).
@@ -134,8 +175,10 @@ fa2_status launch_fwd(const LaunchArgs &a)
     p.part_lse = nullptr;
     p.part_o = nullptr;
     if (p.split) {
-        grid = cut_ranges(units, p.n_kv, static_cast<int>(split_grid(units, p.n_kv, a.num_sms)), ranges.begin,
-                          nullptr);
+        const SplitPlan plan = split_plan(units, p.n_kv, static_cast<int>(split_grid(units, p.n_kv, a.num_sms)));
+        grid = plan.k;
+        for (int c = 0; c <= plan.k; ++c)
+            ranges.begin[c] = plan.begin[c];
         const WorkspaceLayout w = workspace_layout(grid, C::NQ, C::D);
         if (a.workspace_bytes < w.total)
             return FA2_ERR_INVALID_ARG;

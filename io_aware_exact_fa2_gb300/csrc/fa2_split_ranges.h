@@ -105,14 +105,20 @@ inline long long split_grid(long long n_units, long long n_kv, int num_sms)
 // Whether the cost-balanced ranges beat dealing out whole units by at least 5 %:
 // whole units finish after ceil(units / SMs) segments of n_kv tiles; the ranges
 // after the balanced cost plus the merge.
+// (T: the largest range cost cut_ranges found for split_grid(units, n_kv, num_sms) CTAs.)
+inline bool split_pays_given(long long units, long long n_kv, int num_sms, long long T)
+{
+    const long long whole = (units + num_sms - 1) / num_sms * (n_kv + SEGMENT_COST);
+    return (T + MERGE_COST) * 100 < whole * 95;
+}
+
 inline bool split_pays(long long units, long long n_kv, int num_sms)
 {
     if (units * n_kv > INT_MAX)
         return false;
-    const long long whole = (units + num_sms - 1) / num_sms * (n_kv + SEGMENT_COST);
     long long T = 0;
     cut_ranges(units, n_kv, static_cast<int>(split_grid(units, n_kv, num_sms)), nullptr, &T);
-    return (T + MERGE_COST) * 100 < whole * 95;
+    return split_pays_given(units, n_kv, num_sms, T);
 }
 
 }  // namespace fa2
