@@ -48,6 +48,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 
 #include "fa2_split_ranges.h"
@@ -112,6 +113,13 @@ struct FwdCfg {
     // QT: Q lives in TMEM and S = Q K^T takes A from TMEM; the softmax warps copy each
     // Q tile there from shared memory.  Needs one Q tile per unit (TMEM budget).
     static constexpr bool QT = QT_ != 0;
+    // PH: P is handed to the MMA warp in two key halves, so PV on the first half
+    // runs while the softmax computes the second (one warp per row only: with a
+    // column split, a slice's halves are not one contiguous key range)
+#ifndef FA2_P_HALVES
+#define FA2_P_HALVES 1
+#endif
+    static constexpr bool PH = FA2_P_HALVES != 0 && CS_ == 1;
     static constexpr int NCOL = BN / CS;          // S columns per softmax thread
     static constexpr int OCOL = D / CS;           // O columns per softmax thread
     static constexpr int DB = D / 64;             // 64-column (128-byte) swizzle blocks
@@ -143,7 +151,8 @@ struct FwdCfg {
     static constexpr int BAR_DRAIN = BAR_GROUP + NQ;
     static constexpr int BAR_QT_FULL = BAR_DRAIN + 1;        // [2] Q copied into TMEM buffer
     static constexpr int BAR_QT_EMPTY = BAR_QT_FULL + 2;     // [2] last S MMA read the buffer
-    static constexpr int NUM_BARS = BAR_QT_EMPTY + 2;
+    static constexpr int BAR_PA_READY = BAR_QT_EMPTY + 2;    // [NQ][NS] first key half of P written (PH)
+    static constexpr int NUM_BARS = BAR_PA_READY + NQ * NS;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;  // + slack for base alignment
 
@@ -338,6 +347,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         for (int i = 0; i < C::NQ * C::NS; ++i) {
             mbar_init(bar(C::BAR_S_FULL + i), 1);
             mbar_init(bar(C::BAR_P_READY + i), C::GROUP_WARPS);
+            mbar_init(bar(C::BAR_PA_READY + i), C::GROUP_WARPS);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
         for (int q = 0; q < 2; ++q) {
@@ -468,7 +478,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const int q0 = qg * (C::NQ * C::BM);
                 int n_t[C::NQ];
                 int n_max = 0;
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < C::NQ; ++t) {
                     n_t[t] = segment_tiles(sg, q0 + t * C::BM, p, C::BN);
                     n_max = max(n_max, n_t[t]);
@@ -478,7 +488,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 // the last Q tile (highest t) that reads K/V tile j
                 auto last_user = [&](int j) {
                     int lu = 0;
-    #pragma unroll
+#pragma unroll
                     for (int t = 0; t < C::NQ; ++t)
                         if (j < n_t[t])
                             lu = t;
@@ -500,14 +510,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         if constexpr (C::QT) {
                             // A = Q from TMEM buffer qt_buf: 16 bf16 (8 columns) per K step
                             const uint32_t a = tmem + C::TM_Q + qt_buf * (C::D / 2);
-    #pragma unroll
+#pragma unroll
                             for (int kk = 0; kk < C::D / 16; ++kk)
                                 mma_ts(d, a + kk * 8,
                                        dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
                                        C::IDESC_S, kk > 0 ? 1u : 0u);
                         } else {
                             const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
-    #pragma unroll
+#pragma unroll
                             for (int kk = 0; kk < C::D / 16; ++kk)
                                 mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
                                        dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
@@ -527,8 +537,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     const int s = it % C::KS;
                     const uint32_t g = tbase[t] + j;
                     const int b = g % C::NS;
-                    if (!lone_wait(bar(C::BAR_P_READY + t * C::NS + b), (g / C::NS) & 1, p.err, ERR_MMA | 3,
-                                   p.wait_limit_ns))
+                    // with PH, the first key half of P first; the second before its K steps
+                    if (!lone_wait(bar((C::PH ? C::BAR_PA_READY : C::BAR_P_READY) + t * C::NS + b), (g / C::NS) & 1,
+                                   p.err, ERR_MMA | 3, p.wait_limit_ns))
                         return false;
                     if (!lone_wait(bar(C::BAR_V_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
                         return false;
@@ -542,10 +553,20 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         const uint32_t d = tmem + C::TM_O + t * C::D;
                         const uint32_t a = tmem + C::TM_S + (t * C::NS + b) * C::BN;
                         const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
-    #pragma unroll
-                        for (int kk = 0; kk < C::BN / 16; ++kk)
+                        constexpr int KA = C::PH ? C::BN / 32 : C::BN / 16;   // K steps before the second half
+#pragma unroll
+                        for (int kk = 0; kk < KA; ++kk)
                             mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
                                    (j > 0 || kk > 0) ? 1u : 0u);
+                        if constexpr (C::PH) {
+                            if (!lone_wait(bar(C::BAR_P_READY + t * C::NS + b), (g / C::NS) & 1, p.err, ERR_MMA | 7,
+                                           p.wait_limit_ns))
+                                return false;
+                            tc_fence_after();
+#pragma unroll
+                            for (int kk = KA; kk < C::BN / 16; ++kk)
+                                mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV, 1u);
+                        }
                         mma_commit(bar(C::BAR_O_DONE + t));
                         if (last_user(j) == t)
                             mma_commit(bar(C::BAR_V_EMPTY + s));
@@ -555,7 +576,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
                 // this unit's Q tiles: in shared memory (TMA), or copied into TMEM buffer
                 // qt_buf by the softmax warps
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < C::NQ; ++t) {
                     if (ok && n_t[t] > 0) {
                         if constexpr (C::QT)
@@ -570,14 +591,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 // Issue order: S for the first NS tiles of every Q tile, then per K/V
                 // tile j and Q tile t: PV(t, j) followed by S(t, j + NS), which reuses
                 // the TMEM buffer PV(t, j) just read (tcgen05 ops execute in order).
-    #pragma unroll
+#pragma unroll
                 for (int b = 0; b < C::NS; ++b)
-    #pragma unroll
+#pragma unroll
                     for (int t = 0; t < C::NQ; ++t)
                         if (ok && b < n_t[t])
                             ok = issue_s(t, b);
                 for (int j = 0; j < n_max && ok; ++j) {
-    #pragma unroll
+#pragma unroll
                     for (int t = 0; t < C::NQ; ++t) {
                         if (ok && j < n_t[t]) {
                             ok = issue_pv(t, j);
@@ -586,7 +607,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         }
                     }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < C::NQ; ++t) {
                     if (n_t[t] > 0) {
                         tbase[t] += n_t[t];
@@ -760,6 +781,34 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     rescale = true;
                 }
 
+                // Rescale this slice of O (only warps in which some row's max grew) once
+                // the previous PV has landed, before any of this tile's P is handed over,
+                // so that PV(j) accumulates onto the rescaled O.  Without a rescale there
+                // is nothing to wait for: the MMA warp orders PV(j) after PV(j-1) by
+                // itself.  A parity wait on O_DONE is only unambiguous while that barrier
+                // is at most one phase behind the awaited one: here S(j) completing
+                // implies PV(j - NS) completed (and every earlier unit's PVs completed
+                // before its epilogue), so waiting for PV(j-1) is safe; the wait at the
+                // last tile (taken even without a rescale) keeps the epilogue's wait for
+                // PV(n-1) safe too.
+                const bool grow_any = __any_sync(0xffffffffu, rescale);
+                if (j > 0 && grow_any) {
+                    ok = warp_wait(bar(C::BAR_O_DONE + t), (g - 1) & 1, p.err, ERR_SOFTMAX | 2, p.wait_limit_ns);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < C::OCOL / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + 32 * cc, r);
+                        tmem_ld_wait(r);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                        tmem_st32(o_addr + 32 * cc, r);
+                    }
+                }
+
                 // p = 2^(s * scale * log2e - m); masked entries give 2^-inf = 0.  P goes to
                 // TMEM as bf16 (two per 32-bit column, over the first BN/2 columns of the S
                 // buffer; this slice's keys land in columns h*NCOL/2 ..).  Two normalisers
@@ -775,10 +824,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const uint64_t negm2 = f32x2(-m_sub, -m_sub);
                 uint64_t ls01 = 0, ls23 = 0;   // packed (0.f, 0.f)
                 float lr0 = 0.f, lr1 = 0.f;
-                {
-                    uint32_t pk[C::NCOL / 2];
+                uint32_t pk[C::NCOL / 2];
+                const uint32_t p_addr = s_addr + h * (C::NCOL / 2);
+                // weights of columns [CB, CE) into pk (bf16 pairs) and the two sums
+                auto exp_cols = [&](auto cb, auto ce) {
+                    constexpr int CB = decltype(cb)::value, CE = decltype(ce)::value;
 #pragma unroll
-                    for (int c = 0; c < C::NCOL; c += 4) {
+                    for (int c = CB; c < CE; c += 4) {
                         float x0, x1, x2, x3;
                         unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), c2x2, negm2), x0, x1);
                         unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), c2x2, negm2), x2, x3);
@@ -795,14 +847,34 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         lr0 = add_bf16x2_to_f32(lr0, w0);
                         lr1 = add_bf16x2_to_f32(lr1, w1);
                     }
-                    const uint32_t p_addr = s_addr + h * (C::NCOL / 2);
-                    if constexpr (C::NCOL / 2 >= 32) {
+                };
+                // words [W0, W0 + NW) of pk to their TMEM columns
+                auto store_words = [&](auto w0, auto nw) {
+                    constexpr int W0 = decltype(w0)::value, NW = decltype(nw)::value;
+                    static_assert(NW % 32 == 0 || NW == 16, "P stores move 16 or 32 columns at a time");
+                    if constexpr (NW % 32 == 0) {
 #pragma unroll
-                        for (int q = 0; q < C::NCOL / 64; ++q)
-                            tmem_st32(p_addr + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32 * q));
+                        for (int q = 0; q < NW / 32; ++q)
+                            tmem_st32(p_addr + W0 + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pk + W0 + 32 * q));
                     } else {
-                        tmem_st16(p_addr, pk);
+                        tmem_st16(p_addr + W0, pk + W0);
                     }
+                };
+                using Z = std::integral_constant<int, 0>;
+                using HALF = std::integral_constant<int, C::NCOL / 2>;
+                using ALL = std::integral_constant<int, C::NCOL>;
+                if constexpr (C::PH) {
+                    // first key half: stored and handed to the MMA warp before the second
+                    exp_cols(Z{}, HALF{});
+                    store_words(Z{}, std::integral_constant<int, C::NCOL / 4>{});
+                    tmem_st_wait();
+                    tc_fence_before();
+                    warp_arrive(bar(C::BAR_PA_READY + t * C::NS + b));
+                    exp_cols(HALF{}, ALL{});
+                    store_words(std::integral_constant<int, C::NCOL / 4>{}, std::integral_constant<int, C::NCOL / 4>{});
+                } else {
+                    exp_cols(Z{}, ALL{});
+                    store_words(Z{}, HALF{});
                 }
                 {
                     float a0, a1, a2, a3;
@@ -811,33 +883,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     l = l * alpha + ((a0 + a1) + (a2 + a3));
                 }
                 l_o = l_o * alpha + (lr0 + lr1);
-
-                // Rescale this slice of O (only warps in which some row's max grew) once
-                // the previous PV has landed.  Without a rescale there is nothing to wait
-                // for: the MMA warp orders PV(j) after PV(j-1) by itself.  A parity wait on
-                // O_DONE is only unambiguous while that barrier is at most one phase behind
-                // the awaited one: here S(j) completing implies PV(j - NS) completed (and
-                // every earlier unit's PVs completed before its epilogue), so waiting for
-                // PV(j-1) is safe; the wait at the last tile (taken even without a rescale)
-                // keeps the epilogue's wait for PV(n-1) safe too.
-                const bool grow_any = __any_sync(0xffffffffu, rescale);
-                if (j > 0 && (grow_any || j == n - 1)) {
+                if (j > 0 && !grow_any && j == n - 1) {
                     ok = warp_wait(bar(C::BAR_O_DONE + t), (g - 1) & 1, p.err, ERR_SOFTMAX | 2, p.wait_limit_ns);
                     if (!ok)
                         break;
-                    tc_fence_after();
-                    if (grow_any) {
-#pragma unroll 1
-                        for (int cc = 0; cc < C::OCOL / 32; ++cc) {
-                            uint32_t r[32];
-                            tmem_ld32(o_addr + 32 * cc, r);
-                            tmem_ld_wait(r);
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                            tmem_st32(o_addr + 32 * cc, r);
-                        }
-                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
