@@ -113,13 +113,14 @@ struct FwdCfg {
     // QT: Q lives in TMEM and S = Q K^T takes A from TMEM; the softmax warps copy each
     // Q tile there from shared memory.  Needs one Q tile per unit (TMEM budget).
     static constexpr bool QT = QT_ != 0;
-    // PH: P is handed to the MMA warp in two key halves, so PV on the first half
-    // runs while the softmax computes the second (one warp per row only: with a
-    // column split, a slice's halves are not one contiguous key range)
-#ifndef FA2_P_HALVES
-#define FA2_P_HALVES 1
+    // NP: P is handed to the MMA warp in NP key parts, so PV on the earlier parts
+    // runs while the softmax computes the later ones (one warp per row only: with a
+    // column split, a slice's parts are not contiguous key ranges)
+#ifndef FA2_P_PARTS
+#define FA2_P_PARTS 2
 #endif
-    static constexpr bool PH = FA2_P_HALVES != 0 && CS_ == 1;
+    static constexpr int NP = CS_ == 1 ? FA2_P_PARTS : 1;
+    static_assert(NP == 1 || NP == 2 || NP == 4, "P goes over in 1, 2 or 4 parts");
     static constexpr int NCOL = BN / CS;          // S columns per softmax thread
     static constexpr int OCOL = D / CS;           // O columns per softmax thread
     static constexpr int DB = D / 64;             // 64-column (128-byte) swizzle blocks
@@ -151,8 +152,8 @@ struct FwdCfg {
     static constexpr int BAR_DRAIN = BAR_GROUP + NQ;
     static constexpr int BAR_QT_FULL = BAR_DRAIN + 1;        // [2] Q copied into TMEM buffer
     static constexpr int BAR_QT_EMPTY = BAR_QT_FULL + 2;     // [2] last S MMA read the buffer
-    static constexpr int BAR_PA_READY = BAR_QT_EMPTY + 2;    // [NQ][NS] first key half of P written (PH)
-    static constexpr int NUM_BARS = BAR_PA_READY + NQ * NS;
+    static constexpr int BAR_PA_READY = BAR_QT_EMPTY + 2;    // [NQ][NS][NP-1] earlier key parts of P written
+    static constexpr int NUM_BARS = BAR_PA_READY + NQ * NS * (NP > 1 ? NP - 1 : 1);
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;  // + slack for base alignment
 
@@ -347,7 +348,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         for (int i = 0; i < C::NQ * C::NS; ++i) {
             mbar_init(bar(C::BAR_S_FULL + i), 1);
             mbar_init(bar(C::BAR_P_READY + i), C::GROUP_WARPS);
-            mbar_init(bar(C::BAR_PA_READY + i), C::GROUP_WARPS);
+            for (int q = 0; q < C::NP - 1; ++q)
+                mbar_init(bar(C::BAR_PA_READY + i * (C::NP - 1) + q), C::GROUP_WARPS);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
         for (int q = 0; q < 2; ++q) {
@@ -537,9 +539,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     const int s = it % C::KS;
                     const uint32_t g = tbase[t] + j;
                     const int b = g % C::NS;
-                    // with PH, the first key half of P first; the second before its K steps
-                    if (!lone_wait(bar((C::PH ? C::BAR_PA_READY : C::BAR_P_READY) + t * C::NS + b), (g / C::NS) & 1,
-                                   p.err, ERR_MMA | 3, p.wait_limit_ns))
+                    // P arrives in NP key parts: each part's barrier before its K steps
+                    auto part_bar = [&](int q) {
+                        return q < C::NP - 1 ? bar(C::BAR_PA_READY + (t * C::NS + b) * (C::NP - 1) + q)
+                                             : bar(C::BAR_P_READY + t * C::NS + b);
+                    };
+                    if (!lone_wait(part_bar(0), (g / C::NS) & 1, p.err, ERR_MMA | 3, p.wait_limit_ns))
                         return false;
                     if (!lone_wait(bar(C::BAR_V_FULL + s), (it / C::KS) & 1, p.err, ERR_MMA | 4, p.wait_limit_ns))
                         return false;
@@ -553,19 +558,18 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         const uint32_t d = tmem + C::TM_O + t * C::D;
                         const uint32_t a = tmem + C::TM_S + (t * C::NS + b) * C::BN;
                         const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
-                        constexpr int KA = C::PH ? C::BN / 32 : C::BN / 16;   // K steps before the second half
+                        constexpr int KP = C::BN / 16 / C::NP;   // K steps per part of P
 #pragma unroll
-                        for (int kk = 0; kk < KA; ++kk)
-                            mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
-                                   (j > 0 || kk > 0) ? 1u : 0u);
-                        if constexpr (C::PH) {
-                            if (!lone_wait(bar(C::BAR_P_READY + t * C::NS + b), (g / C::NS) & 1, p.err, ERR_MMA | 7,
-                                           p.wait_limit_ns))
-                                return false;
-                            tc_fence_after();
+                        for (int q = 0; q < C::NP; ++q) {
+                            if (q > 0) {
+                                if (!lone_wait(part_bar(q), (g / C::NS) & 1, p.err, ERR_MMA | 7, p.wait_limit_ns))
+                                    return false;
+                                tc_fence_after();
+                            }
 #pragma unroll
-                            for (int kk = KA; kk < C::BN / 16; ++kk)
-                                mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV, 1u);
+                            for (int kk = q * KP; kk < (q + 1) * KP; ++kk)
+                                mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
                         }
                         mma_commit(bar(C::BAR_O_DONE + t));
                         if (last_user(j) == t)
@@ -851,30 +855,35 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 // words [W0, W0 + NW) of pk to their TMEM columns
                 auto store_words = [&](auto w0, auto nw) {
                     constexpr int W0 = decltype(w0)::value, NW = decltype(nw)::value;
-                    static_assert(NW % 32 == 0 || NW == 16, "P stores move 16 or 32 columns at a time");
+                    static_assert(NW % 32 == 0 || NW == 16 || NW == 8, "P stores move 8, 16 or 32 columns at a time");
                     if constexpr (NW % 32 == 0) {
 #pragma unroll
                         for (int q = 0; q < NW / 32; ++q)
                             tmem_st32(p_addr + W0 + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pk + W0 + 32 * q));
-                    } else {
+                    } else if constexpr (NW == 16) {
                         tmem_st16(p_addr + W0, pk + W0);
+                    } else {
+                        tmem_st8(p_addr + W0, pk + W0);
                     }
                 };
-                using Z = std::integral_constant<int, 0>;
-                using HALF = std::integral_constant<int, C::NCOL / 2>;
-                using ALL = std::integral_constant<int, C::NCOL>;
-                if constexpr (C::PH) {
-                    // first key half: stored and handed to the MMA warp before the second
-                    exp_cols(Z{}, HALF{});
-                    store_words(Z{}, std::integral_constant<int, C::NCOL / 4>{});
-                    tmem_st_wait();
-                    tc_fence_before();
-                    warp_arrive(bar(C::BAR_PA_READY + t * C::NS + b));
-                    exp_cols(HALF{}, ALL{});
-                    store_words(std::integral_constant<int, C::NCOL / 4>{}, std::integral_constant<int, C::NCOL / 4>{});
-                } else {
-                    exp_cols(Z{}, ALL{});
-                    store_words(Z{}, HALF{});
+                // part q of NP: its weights, stored, and (all but the last) handed to the
+                // MMA warp before the next part is computed
+                auto part = [&](auto qc) {
+                    constexpr int Q = decltype(qc)::value, PC = C::NCOL / C::NP;
+                    exp_cols(std::integral_constant<int, Q * PC>{}, std::integral_constant<int, (Q + 1) * PC>{});
+                    store_words(std::integral_constant<int, Q * PC / 2>{}, std::integral_constant<int, PC / 2>{});
+                    if constexpr (Q < C::NP - 1) {
+                        tmem_st_wait();
+                        tc_fence_before();
+                        warp_arrive(bar(C::BAR_PA_READY + (t * C::NS + b) * (C::NP - 1) + Q));
+                    }
+                };
+                part(std::integral_constant<int, 0>{});
+                if constexpr (C::NP > 1)
+                    part(std::integral_constant<int, 1>{});
+                if constexpr (C::NP > 2) {
+                    part(std::integral_constant<int, 2>{});
+                    part(std::integral_constant<int, 3>{});
                 }
                 {
                     float a0, a1, a2, a3;
