@@ -77,6 +77,39 @@ fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o,
                    int causal, float scale, void *stream);
 
 /*
+ * fa2_fwd_ex -- the forward pass on strided views ("FlashAttention-2 from
+ * scratch with a custom Triton kernel", host wrapper and kernel launch: the
+ * kernel is given each tensor's batch, head, row and column strides).  Same
+ * computation as fa2_fwd, with an optional sliding window (as fa2_fwd_window)
+ * and workspace (as fa2_fwd_ws).
+ *
+ *   q, k, v, o    bf16 [B, H, L, D] views whose rows of D elements are
+ *                 contiguous; element (b, h, i, d) of q is at
+ *                 q + b*q_strides[0] + h*q_strides[1] + i*q_strides[2] + d,
+ *                 likewise k, v (L = Lk) and o (L = Lq).  A NULL stride array
+ *                 means contiguous [B, H, L, D].  Every stride is in elements,
+ *                 positive and a multiple of 8 (16 bytes; the TMA loads and the
+ *                 16-byte row stores need it), at most 2^38.  The rows of o must
+ *                 not overlap; q, k and v may (e.g. slices of one packed QKV
+ *                 tensor, or [B, L, H, D] storage viewed as [B, H, L, D]).
+ *   lse           fp32 [B, H, Lq] contiguous.
+ *   window        -1: none; w >= 0: causal sliding window, query i sees keys
+ *                 i - w .. i (requires causal and Lq <= Lk, as fa2_fwd_window).
+ *   workspace     optional, as fa2_fwd_ws (used by non-causal calls without a
+ *                 window; 256-byte aligned when given).
+ *   (other arguments as for fa2_fwd)
+ *
+ * Errors as fa2_fwd, plus FA2_ERR_INVALID_ARG for a stride that breaks the
+ * rules above, a bad window or a misaligned workspace.
+ */
+fa2_status fa2_fwd_ex(const void *q, const void *k, const void *v, void *o,
+                      float *lse, int B, int H, int Lq, int Lk, int D,
+                      const long long *q_strides, const long long *k_strides,
+                      const long long *v_strides, const long long *o_strides,
+                      int causal, int window, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
  * fa2_fwd_window -- fa2_fwd for causal attention restricted to a sliding
  * window: query i sees keys i - window <= j <= i ("Flash Attention:
  * principles and implementation" (tbr8.org), section 6.3, window_size =

@@ -46,6 +46,10 @@ def load_library() -> ctypes.CDLL:
     lib.fa2_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa2_fwd_window.restype = i
     lib.fa2_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    ll3 = ctypes.POINTER(ctypes.c_longlong)
+    lib.fa2_fwd_ex.restype = i
+    lib.fa2_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ll3, ll3, ll3, ll3, i, i, f, vp,
+                               ctypes.c_size_t, vp]
     lib.fa2_fwd_noalloc.restype = i
     lib.fa2_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa2_bwd_workspace_size.restype = i
@@ -147,6 +151,44 @@ def fa2_fwd_window(q, k, v, o, lse, window: int, scale: float | None = None, str
                              B, H, Lq, Lk, D, int(window), float(scale), _stream_handle(stream, q.device))
     if st != 0:
         raise Fa2Error(st, "fa2_fwd_window")
+
+
+def fa2_fwd_ex(q, k, v, o, lse, causal: bool, scale: float | None = None, window: int | None = None,
+               workspace=None, stream=None) -> None:
+    """Forward pass on strided (B, H, L, D) views (fa2_fwd_ex).
+
+    q, k, v and o may be any views whose last dimension is contiguous and whose
+    other strides are multiples of 8 elements -- e.g. `x.view(B, L, H, D).transpose(1, 2)`
+    or slices of one packed QKV tensor.  lse must be contiguous (B, H, Lq).
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or o.dim() != 4:
+        raise ValueError("q, k, v, o must be 4-D (B, H, L, D) views")
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    if tuple(k.shape) != (B, H, Lk, D) or tuple(v.shape) != (B, H, Lk, D) or tuple(o.shape) != (B, H, Lq, D):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)} o {tuple(o.shape)}")
+    if tuple(lse.shape) != (B, H, Lq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, Lq) tensor")
+    arrays = []
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if t.stride(3) != 1:
+            raise ValueError(f"{name}'s last dimension must be contiguous")
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+        arrays.append((ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2)))
+    if scale is None:
+        scale = D ** -0.5
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = _lib.fa2_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Lq, Lk, D,
+                         *arrays, int(bool(causal)), -1 if window is None else int(window), float(scale),
+                         ws_ptr, ws_bytes, _stream_handle(stream, q.device))
+    if st != 0:
+        raise Fa2Error(st, "fa2_fwd_ex")
 
 
 def fa2_fwd_noalloc(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:

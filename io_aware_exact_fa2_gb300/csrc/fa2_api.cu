@@ -187,7 +187,7 @@ fa2_status select_device_of(const void *ptr, int *dev_out)
 
 fa2_status launch(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Lq,
                   int Lk, int D, int causal, float scale, cudaStream_t stream, void *workspace = nullptr,
-                  size_t workspace_bytes = 0, int window = -1)
+                  size_t workspace_bytes = 0, int window = -1, const BhlStrides *strides = nullptr)
 {
     int dev = 0;
     fa2_status st = select_device_of(q, &dev);
@@ -203,6 +203,11 @@ fa2_status launch(const void *q, const void *k, const void *v, void *o, float *l
     a.H = H;
     a.Lq = Lq;
     a.Lk = Lk;
+    // Q, K, V, O: the caller's strides, or contiguous [B, H, L, D]
+    a.sq = strides ? strides[0] : contiguous_bhl(H, Lq, D);
+    a.sk = strides ? strides[1] : contiguous_bhl(H, Lk, D);
+    a.sv = strides ? strides[2] : contiguous_bhl(H, Lk, D);
+    a.so = strides ? strides[3] : contiguous_bhl(H, Lq, D);
     a.causal = causal;
     a.window = window;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
@@ -386,6 +391,39 @@ FA2_EXPORT fa2_status fa2_fwd_window(const void *q, const void *k, const void *v
         return FA2_ERR_INVALID_ARG;
     return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, 1, scale, static_cast<cudaStream_t>(stream), nullptr, 0,
                        window);
+}
+
+FA2_EXPORT fa2_status fa2_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                                 int Lq, int Lk, int D, const long long *q_strides, const long long *k_strides,
+                                 const long long *v_strides, const long long *o_strides, int causal, int window,
+                                 float scale, void *workspace, size_t workspace_bytes, void *stream)
+{
+    fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
+    if (st != FA2_OK)
+        return st;
+    if (window < -1 || (window >= 0 && (!causal || Lq > Lk)))
+        return FA2_ERR_INVALID_ARG;
+    if (workspace && !fa2::aligned(workspace, 256))
+        return FA2_ERR_INVALID_ARG;
+    fa2::BhlStrides sts[4] = {fa2::contiguous_bhl(H, Lq, D), fa2::contiguous_bhl(H, Lk, D),
+                              fa2::contiguous_bhl(H, Lk, D), fa2::contiguous_bhl(H, Lq, D)};
+    const long long *given[4] = {q_strides, k_strides, v_strides, o_strides};
+    for (int i = 0; i < 4; ++i) {
+        if (!given[i])
+            continue;
+        // positive, and a multiple of 16 bytes (TMA strides; 16-byte O row stores)
+        for (int d = 0; d < 3; ++d)
+            if (given[i][d] <= 0 || given[i][d] % 8 != 0 || given[i][d] > (1ll << 38))
+                return FA2_ERR_INVALID_ARG;
+        sts[i] = {given[i][0], given[i][1], given[i][2]};
+    }
+    if (Lq == 0)
+        return FA2_OK;
+    if (window >= 0 || causal)   // whole units; the workspace is not used
+        return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, static_cast<cudaStream_t>(stream),
+                           nullptr, 0, window, sts);
+    return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, static_cast<cudaStream_t>(stream), workspace,
+                       workspace_bytes, -1, sts);
 }
 
 FA2_EXPORT fa2_status fa2_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,

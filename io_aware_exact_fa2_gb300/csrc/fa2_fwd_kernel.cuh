@@ -57,8 +57,10 @@
 namespace fa2 {
 
 struct FwdParams {
-    uint16_t *o;                // bf16 [B*H, Lq, D]
+    uint16_t *o;                // bf16 rows of D (row (b, h, i) at b*o_sb + h*o_sh + i*o_sl)
+    long long o_sb, o_sh, o_sl; // O element strides of b, h and the row
     float *lse;                 // fp32 [B*H, Lq]
+    int H;                      // heads (Q/K/V tensor maps are (D, L, H, B))
     int *err;                   // device error word
     unsigned long long wait_limit_ns;
     int Lq, Lk;
@@ -407,8 +409,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         mbar_arrive_expect_tx(bar(C::BAR_Q_FULL + t), C::Q_TILE);
 #pragma unroll
                         for (int c = 0; c < C::DB; ++c)
-                            tma_load_3d_hint(sbase + C::OFF_Q + t * C::Q_TILE + c * C::Q_BLOCK, &tm_q, 64 * c,
-                                             q0 + t * C::BM, bh, bar(C::BAR_Q_FULL + t), pol_q);
+                            tma_load_4d_hint(sbase + C::OFF_Q + t * C::Q_TILE + c * C::Q_BLOCK, &tm_q, 64 * c,
+                                             q0 + t * C::BM, bh % p.H, bh / p.H, bar(C::BAR_Q_FULL + t), pol_q);
                         ++q_loads[t];
                     }
                 }
@@ -422,8 +424,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     mbar_arrive_expect_tx(bar(C::BAR_K_FULL + s), C::KV_TILE);
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
-                        tma_load_3d_hint(sbase + C::OFF_K + s * C::KV_TILE + c * C::KV_BLOCK, &tm_k, 64 * c,
-                                         (sg.kv_lo + j) * C::BN, bh, bar(C::BAR_K_FULL + s), pol_kv);
+                        tma_load_4d_hint(sbase + C::OFF_K + s * C::KV_TILE + c * C::KV_BLOCK, &tm_k, 64 * c,
+                                         (sg.kv_lo + j) * C::BN, bh % p.H, bh / p.H, bar(C::BAR_K_FULL + s), pol_kv);
                     k_pending = true;
                     if (!mbar_wait(bar(C::BAR_V_EMPTY + s), ph ^ 1u, p.err, ERR_PRODUCER | 2, p.wait_limit_ns)) {
                         ok = false;
@@ -432,8 +434,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     mbar_arrive_expect_tx(bar(C::BAR_V_FULL + s), C::KV_TILE);
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
-                        tma_load_3d_hint(sbase + C::OFF_V + s * C::KV_TILE + c * C::KV_BLOCK, &tm_v, 64 * c,
-                                         (sg.kv_lo + j) * C::BN, bh, bar(C::BAR_V_FULL + s), pol_kv);
+                        tma_load_4d_hint(sbase + C::OFF_V + s * C::KV_TILE + c * C::KV_BLOCK, &tm_v, 64 * c,
+                                         (sg.kv_lo + j) * C::BN, bh % p.H, bh / p.H, bar(C::BAR_V_FULL + s), pol_kv);
                     k_pending = false;
                 }
             }
@@ -947,7 +949,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const float inv_l = 1.f / lo_tot;
             const bool live = grow < p.Lq;
             const size_t out_row = static_cast<size_t>(bh) * p.Lq + (live ? grow : 0);
-            uint16_t *orow = p.o + out_row * C::D + h * C::OCOL;
+            uint16_t *orow = p.o + static_cast<long long>(bh / p.H) * p.o_sb +
+                             static_cast<long long>(bh % p.H) * p.o_sh +
+                             static_cast<long long>(live ? grow : 0) * p.o_sl + h * C::OCOL;
             const bool whole = sg.c_first == sg.c_last;
             // this part's workspace rows (cut units only): LSE pairs by row, O as float4
             // column groups of 128 rows each

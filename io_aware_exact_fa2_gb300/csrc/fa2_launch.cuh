@@ -18,11 +18,22 @@ namespace fa2 {
 
 using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
 
+// Element strides of a bf16 [B, H, L, D] view whose rows of D are contiguous.
+struct BhlStrides {
+    long long b, h, l;
+};
+
+inline BhlStrides contiguous_bhl(int H, int L, int D)
+{
+    return {static_cast<long long>(H) * L * D, static_cast<long long>(L) * D, D};
+}
+
 struct LaunchArgs {
     const void *q, *k, *v;
     void *o;
     float *lse;
     int B, H, Lq, Lk;
+    BhlStrides sq, sk, sv, so;   // element strides of Q, K, V, O
     int causal;
     int window;               // causal sliding window, -1: none
     float scale_log2;
@@ -119,6 +130,24 @@ size_t workspace_bytes_for(int B, int H, int Lq, int Lk, int causal, int num_sms
     return workspace_layout(split_grid(units, n_kv, num_sms), C::NQ, C::D).total;
 }
 
+// 4-D view of a bf16 [B, H, L, D] tensor with contiguous rows of D and the given
+// element strides: dims (D, L, H, B) innermost first, a box of 64 columns (128 bytes,
+// one swizzle span) by box_rows rows of one head.  Rows outside [0, L) read as zero.
+inline bool encode_bhld_strided(EncodeTiledFn encode, CUtensorMap *m, const void *ptr, int D, int L, int H, int B,
+                                BhlStrides st, int box_rows)
+{
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.l) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                             static_cast<cuuint64_t>(st.b) * 2};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 3-D view of a contiguous bf16 [B*H, L, D] tensor: dims (D, L, B*H) innermost
 // first, a box of 64 columns (128 bytes, one swizzle span) by box_rows rows by
 // one head.  Rows outside [0, L) of a head read as zero.
@@ -142,13 +171,17 @@ fa2_status launch_fwd(const LaunchArgs &a)
 {
     const int BH = a.B * a.H;
     CUtensorMap tq, tk, tv;
-    if (!encode_bhld(a.encode, &tq, a.q, C::D, a.Lq, BH, C::BM) ||
-        !encode_bhld(a.encode, &tk, a.k, C::D, a.Lk, BH, C::BN) ||
-        !encode_bhld(a.encode, &tv, a.v, C::D, a.Lk, BH, C::BN))
+    if (!encode_bhld_strided(a.encode, &tq, a.q, C::D, a.Lq, a.H, a.B, a.sq, C::BM) ||
+        !encode_bhld_strided(a.encode, &tk, a.k, C::D, a.Lk, a.H, a.B, a.sk, C::BN) ||
+        !encode_bhld_strided(a.encode, &tv, a.v, C::D, a.Lk, a.H, a.B, a.sv, C::BN))
         return FA2_ERR_CUDA;
 
     FwdParams p;
     p.o = static_cast<uint16_t *>(a.o);
+    p.o_sb = a.so.b;
+    p.o_sh = a.so.h;
+    p.o_sl = a.so.l;
+    p.H = a.H;
     p.lse = a.lse;
     p.err = a.err;
     p.wait_limit_ns = a.wait_limit_ns;

@@ -32,7 +32,7 @@ def header_functions():
 
 
 def test_header_declares_the_boundary():
-    assert header_functions() == ["fa2_bwd", "fa2_bwd_workspace_size", "fa2_fwd", "fa2_fwd_from_host",
+    assert header_functions() == ["fa2_bwd", "fa2_bwd_workspace_size", "fa2_fwd", "fa2_fwd_ex", "fa2_fwd_from_host",
                                   "fa2_fwd_noalloc", "fa2_fwd_window", "fa2_fwd_ws", "fa2_get_device_error",
                                   "fa2_status_string", "fa2_version", "fa2_workspace_size"]
 
@@ -173,3 +173,25 @@ def test_window_validation(lib):
     assert f(0, P, P, P, P, 1, 1, 8, 8, 64, 4, 0.125, None) == INVALID
     assert f(P, P, P, P, P, 1, 1, 8, 8, 96, 4, 0.125, None) == UNSUPPORTED
     assert f(P, P, P, P, P, 1, 1, 0, 8, 64, 4, 0.125, None) == OK   # Lq == 0: no-op
+
+
+def test_fwd_ex_validation(lib):
+    """fa2_fwd_ex rejects bad strides, windows and workspaces before any CUDA call."""
+    f = lib.fa2_fwd_ex
+    L3 = ctypes.c_longlong * 3
+
+    def call(qs=None, ks=None, vs=None, os_=None, causal=0, window=-1, ws=None, Lq=8, Lk=8, D=64):
+        arr = [None if s is None else L3(*s) for s in (qs, ks, vs, os_)]
+        return f(P, P, P, P, P, 1, 2, Lq, Lk, D, *arr, causal, window, 0.125, ws, 0, None)
+
+    assert call(Lq=0) == OK                                       # contiguous, Lq == 0: no-op
+    assert call(qs=(2 * 8 * 64, 64, 2 * 64), Lq=0) == OK          # a [B, L, H, D] view of q
+    assert call(qs=(1024, 64, 12)) == INVALID                     # row stride not a multiple of 8
+    assert call(ks=(1024, 0, 64)) == INVALID                      # zero stride
+    assert call(vs=(-1024, 512, 64)) == INVALID                   # negative stride
+    assert call(os_=(1 << 39, 512, 64)) == INVALID                # beyond what a TMA map can address
+    assert call(window=-2) == INVALID
+    assert call(window=4) == INVALID                              # a window needs causal
+    assert call(causal=1, window=4, Lq=9, Lk=8) == INVALID        # and Lq <= Lk
+    assert call(ws=P + 16) == INVALID                             # workspace not 256-byte aligned
+    assert call(D=96) == UNSUPPORTED
