@@ -736,11 +736,20 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const bool band_left = p.window >= 0 && jj * C::BN < q0_t + C::BM - 1 - p.window;
                 if ((p.causal && jj * C::BN + C::BN - 1 > q0_t) || (jj * C::BN + C::BN > p.Lk) || band_left) {
                     const int lim = p.causal ? min(grow + 1, p.Lk) : p.Lk;  // keys < lim are visible
-                    const int lo = p.window >= 0 ? grow - p.window : 0;      // and keys >= lo
+                    // as column bounds of this slice: columns c >= hi are masked, and under a
+                    // window also columns c < lo (c is a constant once the loop is unrolled,
+                    // so each test is one compare against a register)
+                    const int hi = lim - k0;
+                    if (p.window >= 0) {
+                        const int lo = grow - p.window - k0;
 #pragma unroll
-                    for (int c = 0; c < C::NCOL; ++c)
-                        if (k0 + c >= lim || k0 + c < lo)
-                            s[c] = -INFINITY;
+                        for (int c = 0; c < C::NCOL; ++c)
+                            s[c] = (c >= hi || c < lo) ? -INFINITY : s[c];
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < C::NCOL; ++c)
+                            s[c] = c >= hi ? -INFINITY : s[c];
+                    }
                 }
 
                 // row max of this tile (own slice, then the other slices through shared
