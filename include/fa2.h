@@ -218,7 +218,7 @@ fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
 
 /*
  * fa2_bwd_workspace_size -- bytes of device workspace fa2_bwd needs: two fp32
- * per query row (-lse * log2 e and -Delta), rows padded to a multiple of 32
+ * per query row (-lse * log2 e and -Delta), rows padded to a multiple of 64
  * per head.  Returns FA2_OK; FA2_ERR_INVALID_ARG for bad sizes;
  * FA2_ERR_UNSUPPORTED for D other than 64 or 128.
  */

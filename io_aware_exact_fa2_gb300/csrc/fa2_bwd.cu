@@ -8,13 +8,13 @@
 
 namespace fa2 {
 
-// dK/dV: 128 keys resident, query tiles of 32 streamed through a 4-stage ring
-// (dV, dK, two 32-column score pairs and K, V as MMA operands fill TMEM);
+// dK/dV: 128 keys resident, query tiles of 64 streamed through a 4-stage ring
+// (dV, dK and two 64-column score pairs fill TMEM; K and V stay in shared memory);
 // dQ: 128 queries resident, key tiles of 64 through a 4-stage ring.  Two score
 // buffer pairs let one step's MMAs run while the previous step's elementwise
 // work finishes.
 template <int D>
-using BwdKV = BwdCfg<D, 128, 32, 4, 8>;
+using BwdKV = BwdCfg<D, 128, 64, 4, 8>;
 template <int D>
 using BwdQ = BwdCfg<D, 128, 64, 4, 4>;
 static_assert(BWD_STAT_TILE_ROWS == BWD_STAT_ROWS, "workspace sizing and kernels agree on the statistics tiles");

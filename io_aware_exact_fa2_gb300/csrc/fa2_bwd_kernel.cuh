@@ -24,7 +24,7 @@
 //     streamed tiles serve as the MMA's B operand both K-major (for S, dP) and
 //     MN-major (for dV, dK, dQ) without a transpose pass.
 //   * The Delta kernel also writes each query row's -lse * log2 e beside -Delta,
-//     in 32-row tiles, so a streamed query tile's statistics ride one bulk copy
+//     in 64-row tiles, so a streamed query tile's statistics ride one bulk copy
 //     on the same ring barrier as its Q and dO tiles (no global loads in the
 //     producer's loop).
 //   * Every wait is bounded (a device error word records which one ran out).
@@ -41,7 +41,7 @@ namespace fa2 {
 // tiles of BWD_STAT_ROWS query rows: fp32 [B*H][tiles][2][BWD_STAT_ROWS] holding
 // (-lse * log2 e, -Delta) per row, so that one bulk copy brings a streamed query
 // tile's statistics into shared memory.  Rows past Lq hold (-inf, 0): P = 0 there.
-constexpr int BWD_STAT_ROWS = 32;
+constexpr int BWD_STAT_ROWS = 64;
 
 struct BwdParams {
     const float *stats;     // the statistics tiles above
@@ -209,7 +209,8 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, uint16_
 // ============================================================== dK, dV kernel
 // CTA = one tile of RES = 128 keys of one (b, h); steps = query tiles of STR rows.
 // TMEM: dV (D cols), dK (D cols), two S^T buffers and two dP^T buffers (STR cols
-// each; P^T and dS^T overwrite their first STR/2 columns as bf16 pairs).
+// each; P^T and dS^T overwrite half of each elementwise warp's columns as bf16
+// pairs).  The score MMAs read K and V from the resident shared-memory tiles.
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fa2_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -218,14 +219,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 {
     using namespace ptx;
     static_assert(C::STR == BWD_STAT_ROWS, "one statistics tile per streamed query tile");
-    static_assert(C::EW == 8 && C::STR == 32, "two elementwise warps of 16 query columns per lane quarter");
-    // K and V are also copied into TMEM (TM_KA, TM_VA) so that S^T = K Q^T and
-    // dP^T = V dO^T read their A operand from TMEM instead of loading it from
-    // shared memory for every instruction
+    static_assert(C::EW == 8 && C::STR == 64, "two elementwise warps of 32 query columns per lane quarter");
     constexpr int TM_DV = 0, TM_DK = C::D, TM_ST = 2 * C::D, TM_DPT = 2 * C::D + 2 * C::STR;
-    constexpr int TM_KA = 2 * C::D + 4 * C::STR, TM_VA = TM_KA + C::D / 2;
     constexpr int TMEM_COLS = 512;
-    static_assert(TM_VA + C::D / 2 <= TMEM_COLS, "TMEM budget exceeded");
+    static_assert(TM_DPT + 2 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -335,8 +332,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 // 128-byte lines, K = query rows)
                 const uint64_t desc_q_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
                 const uint64_t desc_do_mn = sdesc_sw128(sbase + C::OFF_STR1, C::STR_BLOCK, 1024);
-                // K and V copied into TMEM by the elementwise warps
-                ok = lone_wait(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
+                // the resident K and V tiles as K-major A operands
+                const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
+                const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
+                ok = lone_wait(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
                 tc_fence_after();
                 const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
                 // S^T(b) = K Q^T and dP^T(b) = V dO^T for step s
@@ -348,18 +347,19 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < C::D / 16; ++kk) {
+                        const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4);
                         const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                        mma_ts(tmem + TM_ST + b * C::STR, tmem + TM_KA + kk * 8, desc_q + stage_off(st) + to,
-                               C::IDESC_PAIR, kk > 0 ? 1u : 0u);
-                        mma_ts(tmem + TM_DPT + b * C::STR, tmem + TM_VA + kk * 8, desc_do + stage_off(st) + to,
-                               C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                        mma_ss(tmem + TM_ST + b * C::STR, desc_k + ko, desc_q + stage_off(st) + to, C::IDESC_PAIR,
+                               kk > 0 ? 1u : 0u);
+                        mma_ss(tmem + TM_DPT + b * C::STR, desc_v + ko, desc_do + stage_off(st) + to, C::IDESC_PAIR,
+                               kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(C::BAR_SCORE_FULL + b));
                     return true;
                 };
                 // dV += P^T dO and dK += dS^T Q for step s.  The bf16 pairs of query columns
-                // 16 kk .. 16 kk + 15 sit at column 16 kk of their buffer (8 columns), where
-                // the elementwise warp that owns those queries wrote them.
+                // 16 kk .. 16 kk + 15 sit 8 columns each from the start of the 32 columns of
+                // the elementwise warp that owns those queries, where it wrote them.
                 auto issue_grad = [&](int s) -> bool {
                     const int st = s % C::RING, b = s & 1;
                     if (!lone_wait(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 3,
@@ -370,9 +370,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     for (int kk = 0; kk < C::STR / 16; ++kk) {
                         const uint64_t ko = static_cast<uint64_t>((kk * 16 * 128) >> 4);   // 16 rows
                         const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                        mma_ts(tmem + TM_DV, tmem + TM_ST + b * C::STR + kk * 16, desc_do_mn + stage_off(st) + ko,
+                        const int pc = 32 * (kk >> 1) + 8 * (kk & 1);   // pair column of these queries
+                        mma_ts(tmem + TM_DV, tmem + TM_ST + b * C::STR + pc, desc_do_mn + stage_off(st) + ko,
                                C::IDESC_GRAD, acc);
-                        mma_ts(tmem + TM_DK, tmem + TM_DPT + b * C::STR + kk * 16, desc_q_mn + stage_off(st) + ko,
+                        mma_ts(tmem + TM_DK, tmem + TM_DPT + b * C::STR + pc, desc_q_mn + stage_off(st) + ko,
                                C::IDESC_GRAD, acc);
                     }
                     mma_commit(bar(C::BAR_STR_EMPTY + st));   // this step's Q, dO and stats are free
@@ -394,28 +395,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ elementwise warps
-        // Two warps per 32-lane TMEM quarter: `half` 0 takes query columns 0..15 of
-        // every step (and copies K, stores dV), `half` 1 columns 16..31 (V, dK).
+        // Two warps per 32-lane TMEM quarter: `half` 0 takes query columns 0..31 of
+        // every step (and stores dV), `half` 1 columns 32..63 (and stores dK).
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;         // key row within the tile (TMEM lane)
         const int kj = k0 + row;                     // key index
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const int c0 = 16 * half;                    // this warp's first query column of a step
+        const int c0 = 32 * half;                    // this warp's first query column of a step
         const float c2 = p.scale_log2;
         bool ok = true;
-        if (n_steps > 0) {
-            // this row of K (half 0) or of V (half 1) into TMEM, as a score MMA's A operand
-            ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
-            if (ok) {
-                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + (half ? C::OFF_RES1 : C::OFF_RES0), row,
-                                                      tmem + lane_base + (half ? TM_VA : TM_KA));
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(bar(C::BAR_RES_TMEM));
-            }
-        }
         for (int s = 0; s < n_steps && ok; ++s) {
             const int st = s % C::RING, b = s & 1;
             ok = warp_wait_all(bar(C::BAR_SCORE_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 1, p.wait_limit_ns);
@@ -439,20 +427,21 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const bool need_mask = p.causal && q0 + c0 < k0 + quarter * 32 + 31;
             const uint64_t c2x2 = f32x2(c2, c2);
             const uint64_t zero2 = 0;
-            uint32_t rs[16], rd[16], nl[16], nd[16];
-            tmem_ld16(a_st, rs);
-            tmem_ld16(a_dp, rd);
-            // -lse2 and -Delta of this warp's 16 queries (the same for every lane)
+            uint32_t rs[32], rd[32], nl[32], nd[32];
+            tmem_ld32(a_st, rs);
+            tmem_ld32(a_dp, rd);
+            // -lse2 and -Delta of this warp's 32 queries (the same for every lane)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 8; ++q) {
                 ld_shared_v4(stat + (c0 + 4 * q) * 4, nl[4 * q], nl[4 * q + 1], nl[4 * q + 2], nl[4 * q + 3]);
                 ld_shared_v4(stat + (C::STR + c0 + 4 * q) * 4, nd[4 * q], nd[4 * q + 1], nd[4 * q + 2],
                              nd[4 * q + 3]);
             }
-            tmem_ld_wait(rs, rd);
-            float pv[16], dv[16];
+            tmem_ld_wait(rs);
+            tmem_ld_wait(rd);
+            float pv[32], dv[32];
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
+            for (int e = 0; e < 32; e += 2) {
                 float x0, x1;
                 unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2x2,
                                        f32x2(__uint_as_float(nl[e]), __uint_as_float(nl[e + 1]))),
@@ -465,21 +454,21 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             if (need_mask) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
+                for (int e = 0; e < 32; ++e)
                     if (c0 + e < first_visible) {
                         pv[e] = 0.f;
                         dv[e] = 0.f;
                     }
             }
-            // P^T and dS^T as bf16 pairs over the first 8 of this warp's 16 columns
-            uint32_t pw[8], dw[8];
+            // P^T and dS^T as bf16 pairs over the first 16 of this warp's 32 columns
+            uint32_t pw[16], dw[16];
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
+            for (int e = 0; e < 32; e += 2) {
                 pw[e / 2] = bwd_pack(pv[e], pv[e + 1]);
                 dw[e / 2] = bwd_pack(dv[e], dv[e + 1]);
             }
-            tmem_st8(a_st, pw);
-            tmem_st8(a_dp, dw);
+            tmem_st16(a_st, pw);
+            tmem_st16(a_dp, dw);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();

@@ -254,7 +254,7 @@ struct BwdArgs {
 fa2_status launch_bwd(const BwdArgs &a);
 // Bytes of the backward's statistics tiles: two fp32 per query row, rows padded
 // to a multiple of BWD_STAT_TILE_ROWS per head.
-constexpr int BWD_STAT_TILE_ROWS = 32;
+constexpr int BWD_STAT_TILE_ROWS = 64;
 constexpr size_t bwd_stats_bytes(int B, int H, int Lq)
 {
     return static_cast<size_t>(B) * H * ((static_cast<size_t>(Lq) + BWD_STAT_TILE_ROWS - 1) / BWD_STAT_TILE_ROWS) *
