@@ -16,7 +16,7 @@ namespace fa2 {
 template <int D>
 using BwdKV = BwdCfg<D, 128, 64, 4, 8>;
 template <int D>
-using BwdQ = BwdCfg<D, 128, 64, 4, 4>;
+using BwdQ = BwdCfg<D, 128, 64, 4, 8>;
 static_assert(BWD_STAT_TILE_ROWS == BWD_STAT_ROWS, "workspace sizing and kernels agree on the statistics tiles");
 
 template <class K>

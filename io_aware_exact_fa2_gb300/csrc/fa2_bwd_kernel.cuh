@@ -15,8 +15,9 @@
 //
 // GB300 mapping, per kernel:
 //   * TMA (128B swizzle) moves the resident tiles once and the streamed tiles
-//     through a ring; one warp issues tcgen05.mma (elected lane); four warps
-//     (one TMEM lane = one row each) do the elementwise work.
+//     through a ring; one warp issues tcgen05.mma (elected lane); eight warps
+//     do the elementwise work, two per 32-lane TMEM quarter (one TMEM lane = one
+//     row), each with half of a step's columns.
 //   * The two score-like products of a step (S and dP, or their transposes)
 //     go into one of two TMEM buffer pairs, so the next step's pair is computed
 //     while the elementwise warps work on this one.  P and dS are written back
@@ -500,8 +501,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
 // ================================================================= dQ kernel
 // CTA = one tile of RES = 128 queries of one (b, h); steps = key tiles of STR rows.
-// TMEM: dQ (D cols), two S buffers and two dP buffers (STR cols each; dS
-// overwrites the first STR/2 columns of its S buffer as bf16 pairs).
+// TMEM: dQ (D cols), two S buffers and two dP buffers (STR cols each; each
+// elementwise warp writes the dS pairs of its 32 key columns over the first 16 of
+// them in the S buffer).
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fa2_bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                      const BwdParams p)
 {
     using namespace ptx;
-    static_assert(C::EW == 4, "one elementwise warp per lane quarter");
+    static_assert(C::EW == 8 && C::STR == 64, "two elementwise warps of 32 key columns per lane quarter");
     // Q and dO are also copied into TMEM (TM_QA, TM_DOA) so that S = Q K^T and
     // dP = dO V^T read their A operand from TMEM instead of loading it from shared
     // memory for every instruction
@@ -636,17 +638,21 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 }
                 mma_commit(bar(C::BAR_DP_FULL + b));
             };
-            // dQ += dS K for step s
+            // dQ += dS K for step s.  The bf16 pairs of key columns 16 kk .. 16 kk + 15
+            // sit 8 columns each from the start of the 32 columns of the elementwise
+            // warp that owns those keys, where it wrote them.
             auto issue_grad = [&](int s) -> bool {
                 const int st = s % C::RING, b = s & 1;
                 if (!lone_wait(bar(C::BAR_GRAD_READY + b), (s >> 1) & 1, p.err, ERR_BWD_MMA | 7, p.wait_limit_ns))
                     return false;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < C::STR / 16; ++kk)
-                    mma_ts(tmem + TM_DQ, tmem + TM_S + b * C::STR + kk * 8,
+                for (int kk = 0; kk < C::STR / 16; ++kk) {
+                    const int pc = 32 * (kk >> 1) + 8 * (kk & 1);   // pair column of these keys
+                    mma_ts(tmem + TM_DQ, tmem + TM_S + b * C::STR + pc,
                            desc_k_mn + stage_off(st) + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::IDESC_GRAD,
                            (s > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(bar(C::BAR_STR_EMPTY + st));
                 return true;
             };
@@ -672,9 +678,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         __syncwarp();
     } else {
-        const int row = warp * 32 + lane;            // query row within the tile
+        // ------------------------------------------------ elementwise warps
+        // Two warps per 32-lane TMEM quarter: `half` 0 takes key columns 0..31 of
+        // every step, `half` 1 columns 32..63; each stores half of dQ's columns.
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;         // query row within the tile (TMEM lane)
         const int qi = q0 + row;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const int c0 = 32 * half;                    // this warp's first key column of a step
         const float c2 = p.scale_log2;
         const bool live = qi < p.Lq;
         const size_t srow = static_cast<size_t>(bh) * p.Lq + (live ? qi : 0);
@@ -685,47 +696,48 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const float dl = live ? -stat[BWD_STAT_ROWS] : 0.f;
         // keys j < lim are visible to this row
         const int lim = p.causal ? min(qi + 1, p.Lk) : p.Lk;
-        // this row of Q and of dO into TMEM, as the score MMAs' A operands
+        // this row of Q (half 0) or of dO (half 1) into TMEM, as a score MMA's A operand
         bool ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
         if (ok) {
-            copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_QA);
-            copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES1, row, tmem + lane_base + TM_DOA);
+            if (half == 0)
+                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_QA);
+            else
+                copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES1, row, tmem + lane_base + TM_DOA);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(C::BAR_RES_TMEM));
         }
+        const uint64_t c2x2 = f32x2(c2, c2);
+        const uint64_t nl2 = f32x2(-lse2, -lse2);
+        const uint64_t nd2 = f32x2(-dl, -dl);
+        const uint64_t zero2 = 0;
         for (int s = 0; s < n_steps && ok; ++s) {
             const int b = s & 1;
             ok = warp_wait_all(bar(C::BAR_SCORE_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 3, p.wait_limit_ns);
             if (!ok)
                 break;
             tc_fence_after();
-            const uint32_t a_s = tmem + lane_base + TM_S + b * C::STR;
-            const uint32_t a_dp = tmem + lane_base + TM_DP + b * C::STR;
-            const int j0 = s * C::STR;
+            const uint32_t a_s = tmem + lane_base + TM_S + b * C::STR + c0;
+            const uint32_t a_dp = tmem + lane_base + TM_DP + b * C::STR + c0;
+            const int j0 = s * C::STR + c0;          // this warp's first key
             // key columns at or past lim are masked; only a tile reaching lim for some
             // row of this warp needs the per-element test
-            const bool need_mask = __any_sync(0xffffffffu, j0 + C::STR > lim);
-            const uint64_t c2x2 = f32x2(c2, c2);
-            const uint64_t nl2 = f32x2(-lse2, -lse2);
-            const uint64_t nd2 = f32x2(-dl, -dl);
-            const uint64_t zero2 = 0;
-            // P = 2^(S c - lse2) for the whole tile, before dP is needed
-            float pv[C::STR];
-#pragma unroll
-            for (int ch = 0; ch < C::STR / 32; ++ch) {
+            const bool need_mask = __any_sync(0xffffffffu, j0 + 32 > lim);
+            // P = 2^(S c - lse2) for this warp's 32 keys, before dP is needed
+            float pv[32];
+            {
                 uint32_t rs[32];
-                tmem_ld32(a_s + 32 * ch, rs);
+                tmem_ld32(a_s, rs);
                 tmem_ld_wait(rs);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float x0, x1;
                     unpack_f32x2(fma_f32x2(f32x2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2x2, nl2), x0,
                                  x1);
-                    pv[32 * ch + e] = ex2_approx(x0);
-                    pv[32 * ch + e + 1] = ex2_approx(x1);
+                    pv[e] = ex2_approx(x0);
+                    pv[e + 1] = ex2_approx(x1);
                 }
             }
             // dS = P (dP - Delta), once dP is in
@@ -733,46 +745,38 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (!ok)
                 break;
             tc_fence_after();
-            uint32_t dw[C::STR / 2];
+            uint32_t rd[32];
+            tmem_ld32(a_dp, rd);
+            tmem_ld_wait(rd);
+            float dv[32];
 #pragma unroll
-            for (int ch = 0; ch < C::STR / 32; ++ch) {
-                uint32_t rd[32];
-                tmem_ld32(a_dp + 32 * ch, rd);
-                tmem_ld_wait(rd);
-                float dv[32];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const uint64_t diff = add_f32x2(f32x2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])), nd2);
-                    unpack_f32x2(fma_f32x2(f32x2(pv[32 * ch + e], pv[32 * ch + e + 1]), diff, zero2), dv[e],
-                                 dv[e + 1]);
-                }
-                if (need_mask) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (j0 + 32 * ch + e >= lim)
-                            dv[e] = 0.f;
-                }
-#pragma unroll
-                for (int e = 0; e < 32; e += 2)
-                    dw[(32 * ch + e) / 2] = bwd_pack(dv[e], dv[e + 1]);
+            for (int e = 0; e < 32; e += 2) {
+                const uint64_t diff = add_f32x2(f32x2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])), nd2);
+                unpack_f32x2(fma_f32x2(f32x2(pv[e], pv[e + 1]), diff, zero2), dv[e], dv[e + 1]);
             }
-            // dS as bf16 pairs over the first STR/2 columns of the S buffer
-            if constexpr (C::STR / 2 >= 32) {
+            if (need_mask) {
+                const int hi = lim - j0;             // columns c >= hi are masked
 #pragma unroll
-                for (int q = 0; q < C::STR / 64; ++q)
-                    tmem_st32(a_s + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(dw + 32 * q));
-            } else {
-                tmem_st16(a_s, dw);
+                for (int e = 0; e < 32; ++e)
+                    dv[e] = e >= hi ? 0.f : dv[e];
             }
+            // dS as bf16 pairs over the first 16 of this warp's 32 columns of the S buffer
+            uint32_t dw[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+                dw[e / 2] = bwd_pack(dv[e], dv[e + 1]);
+            tmem_st16(a_s, dw);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(C::BAR_GRAD_READY + b));
         }
+        // epilogue: scale * dQ, columns [half * D/2, (half + 1) * D/2) of this row
         if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 4, p.wait_limit_ns)) {
             tc_fence_after();
-            store_acc_row<C::D>(tmem + lane_base + TM_DQ, p.scale, p.dq + srow * C::D, live);
+            store_acc_row<C::D / 2>(tmem + lane_base + TM_DQ + half * (C::D / 2), p.scale,
+                                    p.dq + srow * C::D + half * (C::D / 2), live);
         }
     }
 
