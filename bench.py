@@ -215,6 +215,11 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# tile configuration of the forward kernel per head dimension (fa2_fwd_d*.cu defaults)
+FWD_KERNEL_LABEL = {64: "fa2::fwd_kernel<D=64,BN=128,NQ=2>", 128: "fa2::fwd_kernel<D=128,BN=128,NQ=2>",
+                    256: "fa2::fwd_kernel<D=256,BN=64,NQ=1,Q in TMEM>"}
+
+
 def workload_config(w):
     return {"workload": f"{w.name}: B{w.B} H{w.H} Lq{w.Lq} Lk{w.Lk} D{w.D} bf16, "
                         + " + ".join(w.modes) + " per step",
@@ -306,6 +311,19 @@ def run_ours(args, world, rank, local):
     in_bytes = (q.numel() + k.numel() + v.numel()) * 2
     out_bytes = o.numel() * 2 + lse.numel() * 4
 
+    # the host link itself (what bounds the end-to-end number): plain pinned copies of
+    # Q in and O out, three of each, CUDA events on the same stream
+    def link_gbs(dst, src):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        dst.copy_(src, non_blocking=True)
+        ev[0].record(stream)
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        return 3 * src.numel() * src.element_size() / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+    link = {"h2d_gbs": link_gbs(qd, qh), "d2h_gbs": link_gbs(oh, o)}
+
     # ---- backward pass (context, not the headline metric): its own timed region
     backward = None
     if not args.no_backward and w.D in (64, 128):
@@ -360,14 +378,14 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / peak,
                      "peak_source": f"{peak_src} bf16_tflops (burst: each launch is timed alone)",
                      "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
-                     "kernel": "fa2::fwd_kernel<D=128,BN=128,NQ=2>"},
+                     "kernel": FWD_KERNEL_LABEL[w.D]},
         "per_mode": per_mode,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": in_bytes * len(modes),
                 "d2h_bytes_per_step": out_bytes * len(modes),
                 "how": "fa2_fwd_from_host per mode: pinned host -> device copies, kernels "
                        "(whole-query-tile schedule) and device -> host copies of O and LSE, "
-                       "overlapped over chunks of heads, all inside the CUDA-event region; "
-                       "this box's host link moves about 210 GB/s in and 193 GB/s out"},
+                       "overlapped over chunks of heads, all inside the CUDA-event region",
+                "host_link_gbs": link},
         "gpu_launches": args.steps * len(modes),
         "clocks": clocks,
     }
