@@ -71,7 +71,8 @@ static fa2_status launch_bwd_d(const BwdArgs &a)
         return FA2_ERR_CUDA;
     if (a.Lq > 0) {
         const long long rows = static_cast<long long>(BH) * n_stat_tiles * BWD_STAT_ROWS;
-        fa2_bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, a.stream>>>(
+        constexpr int rpb = bwd_delta_rows_per_block<D>();
+        fa2_bwd_delta_kernel<D><<<static_cast<unsigned>((rows + rpb - 1) / rpb), BWD_DELTA_THREADS, 0, a.stream>>>(
             static_cast<const uint16_t *>(a.o), static_cast<const uint16_t *>(a.dout), a.lse, a.stats, a.Lq,
             n_stat_tiles, rows);
         const long long n_qt = (a.Lq + CQ::RES - 1) / CQ::RES;

@@ -75,42 +75,53 @@ __device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, int
 }
 
 // ---------------------------------------------------------------- Delta (6.2)
-// One warp per query row, padded rows included: Delta = sum_d dO * O in fp32 from
-// the bf16 tensors, stored negated beside -lse * log2 e in the statistics tiles.
+// Delta = sum_d dO * O in fp32 from the bf16 tensors, for every query row (padded
+// rows included), stored negated beside -lse * log2 e in the statistics tiles.  A
+// row is D/8 lanes, each with one 16-byte piece of O and of dO, so a warp covers
+// 32 / (D/8) rows with two vector loads per lane.
+constexpr int BWD_DELTA_THREADS = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256) fa2_bwd_delta_kernel(const uint16_t *__restrict__ o,
-                                                            const uint16_t *__restrict__ dout,
-                                                            const float *__restrict__ lse,
-                                                            float *__restrict__ stats, int Lq, int n_tiles,
-                                                            long long rows)
+__host__ __device__ constexpr int bwd_delta_rows_per_block()
 {
-    const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    return (BWD_DELTA_THREADS / 32) * (32 / (D / 8));
+}
+
+template <int D>
+__global__ void __launch_bounds__(BWD_DELTA_THREADS) fa2_bwd_delta_kernel(const uint16_t *__restrict__ o,
+                                                                          const uint16_t *__restrict__ dout,
+                                                                          const float *__restrict__ lse,
+                                                                          float *__restrict__ stats, int Lq,
+                                                                          int n_tiles, long long rows)
+{
+    constexpr int LPR = D / 8;            // lanes per row
     const int lane = threadIdx.x & 31;
-    if (r >= rows)
-        return;
+    const int piece = lane % LPR;
+    const long long r = static_cast<long long>(blockIdx.x) * bwd_delta_rows_per_block<D>() +
+                        (threadIdx.x >> 5) * (32 / LPR) + lane / LPR;
     const long long per_head = static_cast<long long>(n_tiles) * BWD_STAT_ROWS;
     const long long bh = r / per_head;
     const int i = static_cast<int>(r - bh * per_head);
-    float acc = 0.f, neg_lse2 = -INFINITY;
-    if (i < Lq) {
-        const long long src = bh * Lq + i;
-        constexpr int PER = D / 32;   // elements per lane (2 or 4)
-        const uint16_t *orow = o + src * D + lane * PER;
-        const uint16_t *drow = dout + src * D + lane * PER;
+    const bool live = r < rows && i < Lq;
+    float acc = 0.f;
+    if (live) {
+        const long long src = (bh * Lq + i) * D + piece * 8;
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(o + src));
+        const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dout + src));
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            const float a = __uint_as_float(static_cast<uint32_t>(orow[e]) << 16);
-            const float b = __uint_as_float(static_cast<uint32_t>(drow[e]) << 16);
-            acc = fmaf(a, b, acc);
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
+            acc = fmaf(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wb[e] & 0xffff0000u), acc);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        neg_lse2 = -(lse[src] * BWD_LOG2E);
     }
-    if (lane == 0) {
+    // sum over the row's lanes (xor offsets below LPR stay within the row's group)
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (piece == 0 && r < rows) {
         float *t = stats + (bh * n_tiles + i / BWD_STAT_ROWS) * 2 * BWD_STAT_ROWS + i % BWD_STAT_ROWS;
-        t[0] = neg_lse2;
+        t[0] = i < Lq ? -(lse[bh * Lq + i] * BWD_LOG2E) : -INFINITY;
         t[BWD_STAT_ROWS] = i < Lq ? -acc : 0.f;
     }
 }
