@@ -87,6 +87,18 @@ def test_causal_unequal_lengths(Lq, Lk):
         assert torch.count_nonzero(got[1][:, :, Lq:]) == 0 and torch.count_nonzero(got[2][:, :, Lq:]) == 0
 
 
+@pytest.mark.parametrize("D,causal", [(64, True), (64, False), (128, True)], ids=["d64-causal", "d64-noncausal", "d128-causal"])
+def test_more_key_tiles_than_sms(D, causal):
+    """More key tiles (5 per head x 64 heads) than SMs, so the dK/dV grid runs in
+    several waves; when causal with Lk > Lq, tiles no query sees (zero gradients, no
+    MMAs) sit between tiles with steps in every wave."""
+    Lq, Lk = 200, 600
+    inputs, got = run_bwd(1, 64, Lq, Lk, D, causal, seed=5600 + D)
+    compare_grads(inputs, got, causal, heads=[0, 17, 38, 63])
+    if causal:
+        assert torch.count_nonzero(got[1][:, :, Lq:]) == 0 and torch.count_nonzero(got[2][:, :, Lq:]) == 0
+
+
 def test_many_heads_and_large_dout():
     """More CTAs than SMs in both kernels, and a dO of larger magnitude (x16, exact in bf16)."""
     inputs, got = run_bwd(4, 16, 320, 320, 64, False, seed=5400, dout_scale=16.0)
