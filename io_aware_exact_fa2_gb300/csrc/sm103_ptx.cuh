@@ -167,17 +167,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
-// Same, with an L2 cache-policy hint (from createpolicy).
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, int c0, int c1,
-                                                 int c2, uint32_t bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 // 4-D tiled load global -> shared with an L2 cache-policy hint, completion counted on
 // `bar` in bytes.
 __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3,
@@ -204,23 +193,6 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
-// 3-D tiled store shared -> global; elements outside the tensor are skipped.
-__device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2, uint32_t src)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-            reinterpret_cast<uint64_t>(tmap)),
-        "r"(c0), "r"(c1), "r"(c2), "r"(src)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-__device__ __forceinline__ void tma_store_wait_read_all()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // Release this thread's prior writes / acquire others' at GPU scope (cumulative
 // over what this thread has observed, e.g. through a CTA barrier).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -230,12 +202,6 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *ptr)
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
     return v;
-}
-
-// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -312,31 +278,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 // Wait for all of this thread's outstanding TMEM loads.  The registers of `r`
 // are threaded through as in/out operands so the compiler cannot move any
 // use of them above the wait.
-// 32 lanes x 16 columns of 32 bits (one column per register)
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-                 "%12, %13, %14, %15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                   "=r"(r[14]), "=r"(r[15])
-                 : "r"(taddr)
-                 : "memory");
-}
-
-// Wait for this thread's outstanding TMEM loads into two 16-register arrays.
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&a)[16], uint32_t (&b)[16])
-{
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
-                   "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]),
-                   "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]),
-                   "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]),
-                   "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
-                 :
-                 : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32])
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
@@ -522,12 +463,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d)
 {
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
 }
 
 }  // namespace ptx
