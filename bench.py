@@ -352,6 +352,26 @@ def run_ours(args, world, rank, local):
             raise RuntimeError(f"device error {st} code {code:#x} in the backward pass")
         backward = (bwd_ms, )
 
+    # ---- sliding-window pass (context): causal with keys i - window <= j <= i
+    window = None
+    if args.window is not None and w.Lq <= w.Lk:
+        from io_aware_exact_fa2_gb300 import fa2_fwd_window
+        for _ in range(max(3, args.warmup)):
+            fa2_fwd_window(qd, kd, vd, o, lse, args.window, w.scale, stream=stream)
+        evw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier(world)
+        for s_ in range(args.steps):
+            flush.fill_(float(s_))
+            evw[s_][0].record(stream)
+            fa2_fwd_window(qd, kd, vd, o, lse, args.window, w.scale, stream=stream)
+            evw[s_][1].record(stream)
+        torch.cuda.synchronize(dev)
+        st, code = fa2_get_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error {st} code {code:#x} in the windowed pass")
+        window = (args.window, max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evw])), world, dev))
+
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
@@ -404,7 +424,21 @@ def run_ours(args, world, rank, local):
             "unit": UNIT, "per_mode": bwd,
             "kernels": "Delta, dQ (query tiles resident), dK/dV (key tiles resident) per call (fa2_bwd)",
             "l2": "flushed (256 MiB write) before every timed call"}
+    if window is not None:
+        wv, ms = window
+        tf = window_flops(w, wv) / (ms * 1e-3) / 1e12
+        line["window"] = {
+            "metric": "sliding-window attention fwd TFLOP/s, FLOPs = 4 D per visible (query, key) pair",
+            "window": wv, "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "unit": UNIT,
+            "l2": "flushed (256 MiB write) before every timed launch"}
     print(json.dumps(line), flush=True)
+
+
+def window_flops(w, window: int) -> float:
+    """4 * D FLOPs per visible pair: query i sees keys max(0, i - window) .. i (Lq <= Lk)."""
+    lq, n = w.Lq, window + 1
+    pairs = lq * (lq + 1) // 2 if lq <= n else n * (n + 1) // 2 + (lq - n) * n
+    return 4.0 * w.B * w.H * w.D * pairs
 
 
 def main():
@@ -418,6 +452,8 @@ def main():
                     help="seconds of oracle work for the cpu_baseline field")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass timing")
+    ap.add_argument("--window", type=int, default=None,
+                    help="also time the sliding-window pass with this window (keys i - window .. i)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -17,6 +17,21 @@ import bench  # noqa: E402
 from io_aware_exact_fa2_gb300.workloads import WORKLOADS  # noqa: E402
 
 
+def test_window_flops_count_visible_pairs():
+    """Sliding window: 4*D FLOPs per visible pair, query i seeing keys max(0, i - w) .. i;
+    checked against a direct count, and w >= Lq - 1 equals the causal count plus the diagonal."""
+    class W:
+        B, H, D = 2, 3, 64
+    for lq, win in [(1, 0), (5, 0), (5, 2), (5, 4), (5, 10), (300, 100), (129, 128)]:
+        W.Lq = lq
+        direct = sum(min(i, win) + 1 for i in range(lq))
+        assert bench.window_flops(W, win) == 4 * W.B * W.H * W.D * direct
+    c4 = WORKLOADS["c4"]
+    full = bench.window_flops(c4, c4.Lq)
+    assert full == 4 * c4.B * c4.H * c4.D * c4.Lq * (c4.Lq + 1) // 2
+    assert full - c4.flops(True) == 4 * c4.B * c4.H * c4.D * c4.Lq / 2
+
+
 def test_flop_and_byte_counts():
     """FLOPs = 4*B*H*Lq*Lk*D (halved for causal); bytes = Q,K,V read once + O, LSE written once."""
     c3 = WORKLOADS["c3"]
