@@ -370,7 +370,31 @@ def run_ours(args, world, rank, local):
         st, code = fa2_get_device_error(stream)
         if st != 0:
             raise RuntimeError(f"device error {st} code {code:#x} in the windowed pass")
-        window = (args.window, max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evw])), world, dev))
+        fwd_w_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evw])), world, dev)
+        bwd_w_ms = None
+        if not args.no_backward and w.D in (64, 128):
+            from io_aware_exact_fa2_gb300 import fa2_bwd_window, fa2_bwd_workspace_size
+            g = torch.Generator(device="cpu").manual_seed(w.seed_base + 7)
+            dout = torch.randn(w.B, w.H, w.Lq, w.D, generator=g).to(torch.bfloat16).to(dev)
+            dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+            bws = torch.empty(max(fa2_bwd_workspace_size(w.B, w.H, w.Lq, w.Lk, w.D), 16), dtype=torch.uint8,
+                              device=dev)
+            fa2_fwd_window(qd, kd, vd, o, lse, args.window, w.scale, stream=stream)
+            for _ in range(max(2, args.warmup)):
+                fa2_bwd_window(qd, kd, vd, o, lse, dout, dq, dk, dv, args.window, w.scale, stream=stream,
+                               workspace=bws)
+            for s_ in range(args.steps):
+                flush.fill_(float(s_))
+                evw[s_][0].record(stream)
+                fa2_bwd_window(qd, kd, vd, o, lse, dout, dq, dk, dv, args.window, w.scale, stream=stream,
+                               workspace=bws)
+                evw[s_][1].record(stream)
+            torch.cuda.synchronize(dev)
+            st, code = fa2_get_device_error(stream)
+            if st != 0:
+                raise RuntimeError(f"device error {st} code {code:#x} in the windowed backward pass")
+            bwd_w_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evw])), world, dev)
+        window = (args.window, fwd_w_ms, bwd_w_ms)
 
     if rank != 0:
         return
@@ -425,12 +449,16 @@ def run_ours(args, world, rank, local):
             "kernels": "Delta, dQ (query tiles resident), dK/dV (key tiles resident) per call (fa2_bwd)",
             "l2": "flushed (256 MiB write) before every timed call"}
     if window is not None:
-        wv, ms = window
+        wv, ms, bms = window
         tf = window_flops(w, wv) / (ms * 1e-3) / 1e12
         line["window"] = {
             "metric": "sliding-window attention fwd TFLOP/s, FLOPs = 4 D per visible (query, key) pair",
             "window": wv, "ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "unit": UNIT,
             "l2": "flushed (256 MiB write) before every timed launch"}
+        if bms is not None:
+            btf = 2.5 * window_flops(w, wv) / (bms * 1e-3) / 1e12
+            line["window"]["backward"] = {"ms": bms, "tflops": btf, "frac_of_peak": btf / peak,
+                                          "flops": "2.5 x the windowed forward's (fa2_bwd_window)"}
     print(json.dumps(line), flush=True)
 
 

@@ -257,6 +257,24 @@ fa2_status fa2_bwd(const void *q, const void *k, const void *v, const void *o,
                    void *stream);
 
 /*
+ * fa2_bwd_window -- the backward pass of fa2_fwd_window's sliding-window
+ * attention ("Flash Attention: principles and implementation", section 6.3,
+ * window_size = (window, 0) with causal): query i sees keys
+ * max(0, i - window) .. i only, so P, dS and the gradients are those of that
+ * mask.  o and lse must be fa2_fwd_window's outputs for the same window.
+ * dk and dv rows of keys that no query sees are zero.
+ *
+ *   window       >= 0; Lq <= Lk (as fa2_fwd_window).
+ *   (other arguments, workspace and errors as fa2_bwd; FA2_ERR_INVALID_ARG for
+ *   window < 0 or Lq > Lk)
+ */
+fa2_status fa2_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                          const float *lse, const void *dout, void *dq, void *dk,
+                          void *dv, int B, int H, int Lq, int Lk, int D, int window,
+                          float scale, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
  * fa2_fwd_from_host -- the same pass starting from, and ending in, HOST
  * memory: copies q, k, v from the host into the caller's device staging
  * buffers, runs the pass, and copies O and LSE back into the caller's host

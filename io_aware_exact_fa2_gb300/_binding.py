@@ -56,6 +56,8 @@ def load_library() -> ctypes.CDLL:
     lib.fa2_bwd_workspace_size.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
     lib.fa2_bwd.restype = i
     lib.fa2_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.fa2_bwd_window.restype = i
+    lib.fa2_bwd_window.argtypes = [vp] * 9 + [i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa2_get_device_error.restype = i
     lib.fa2_get_device_error.argtypes = [vp, ctypes.POINTER(i)]
     lib.fa2_status_string.restype = ctypes.c_char_p
@@ -222,6 +224,16 @@ def fa2_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None =
     workspace: a float32/uint8 CUDA tensor of at least fa2_bwd_workspace_size bytes
     (allocated here when not given).
     """
+    _bwd(q, k, v, o, lse, do, dq, dk, dv, bool(causal), None, scale, stream, workspace)
+
+
+def fa2_bwd_window(q, k, v, o, lse, do, dq, dk, dv, window: int, scale: float | None = None, stream=None,
+                   workspace=None) -> None:
+    """Backward pass of fa2_fwd_window (causal, query i sees keys i - window .. i; Lq <= Lk)."""
+    _bwd(q, k, v, o, lse, do, dq, dk, dv, True, int(window), scale, stream, workspace)
+
+
+def _bwd(q, k, v, o, lse, do, dq, dk, dv, causal, window, scale, stream, workspace) -> None:
     import torch
     B, H, Lq, Lk, D = _check_shapes(q, k, v, o, lse)
     for name, t, shape in (("do", do, (B, H, Lq, D)), ("dq", dq, (B, H, Lq, D)), ("dk", dk, (B, H, Lk, D)),
@@ -236,12 +248,17 @@ def fa2_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None =
     n = fa2_bwd_workspace_size(B, H, Lq, Lk, D)
     if workspace is None:
         workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
-    st = _lib.fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
-                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq, Lk, D, int(bool(causal)), float(scale),
-                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                      _stream_handle(stream, q.device))
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if window is None:
+        st = _lib.fa2_bwd(*ptrs, B, H, Lq, Lk, D, int(causal), float(scale), *ws)
+        name = "fa2_bwd"
+    else:
+        st = _lib.fa2_bwd_window(*ptrs, B, H, Lq, Lk, D, window, float(scale), *ws)
+        name = "fa2_bwd_window"
     if st != 0:
-        raise Fa2Error(st, "fa2_bwd")
+        raise Fa2Error(st, name)
 
 
 def fa2_bwd_workspace_size(B: int, H: int, Lq: int, Lk: int, D: int) -> int:

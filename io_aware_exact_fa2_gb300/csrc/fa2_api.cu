@@ -324,9 +324,12 @@ FA2_EXPORT fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D
     return FA2_OK;
 }
 
-FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-                              const void *dout, void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D,
-                              int causal, float scale, void *workspace, size_t workspace_bytes, void *stream)
+namespace fa2 {
+namespace {
+// The backward pass; window >= 0 (causal only) restricts query i to keys i - window .. i.
+fa2_status bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+               void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D, int causal, int window, float scale,
+               void *workspace, size_t workspace_bytes, void *stream)
 {
     // the forward's own checks cover q, k, v, o, lse, sizes and scale
     fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
@@ -370,6 +373,7 @@ FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const
     a.Lk = Lk;
     a.D = D;
     a.causal = causal;
+    a.window = window;
     a.scale = scale;
     a.err = fa2::device_error_ptr(dev);
     a.wait_limit_ns = fa2::wait_limit_ns();
@@ -379,6 +383,27 @@ FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const
     if (!a.err || !a.encode)
         return FA2_ERR_CUDA;
     return fa2::launch_bwd(a);
+}
+}  // namespace
+}  // namespace fa2
+
+FA2_EXPORT fa2_status fa2_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                              const void *dout, void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D,
+                              int causal, float scale, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return fa2::bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, D, causal, -1, scale, workspace,
+                    workspace_bytes, stream);
+}
+
+FA2_EXPORT fa2_status fa2_bwd_window(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                                     const void *dout, void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk,
+                                     int D, int window, float scale, void *workspace, size_t workspace_bytes,
+                                     void *stream)
+{
+    if (window < 0 || Lq > Lk)
+        return FA2_ERR_INVALID_ARG;
+    return fa2::bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, D, 1, window, scale, workspace,
+                    workspace_bytes, stream);
 }
 
 FA2_EXPORT fa2_status fa2_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B,

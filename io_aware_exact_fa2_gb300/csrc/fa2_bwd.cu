@@ -62,6 +62,7 @@ static fa2_status launch_bwd_d(const BwdArgs &a)
     p.Lk = a.Lk;
     p.BH = BH;
     p.causal = a.causal ? 1 : 0;
+    p.window = a.causal ? a.window : -1;
     p.scale = a.scale;
     p.scale_log2 = a.scale * BWD_LOG2E;
 

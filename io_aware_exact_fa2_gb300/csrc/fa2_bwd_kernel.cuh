@@ -53,6 +53,7 @@ struct BwdParams {
     unsigned long long wait_limit_ns;
     int Lq, Lk, BH;
     int causal;
+    int window;             // >= 0 (with causal): query i sees keys i - window .. i; -1: no window
     float scale;            // softmax scale (dK, dQ carry it)
     float scale_log2;       // scale * log2(e)
 };
@@ -253,7 +254,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // causal (top-left): query i sees key j iff j <= i, so query tiles before the
     // one holding row k0 see none of these keys
     const int qt0 = p.causal ? min(k0 / C::STR, n_qt) : 0;
-    const int n_steps = n_qt - qt0;
+    // under a sliding window only queries up to the last key + window see these keys
+    const int qt_end = p.window >= 0 ? min(n_qt, (k0 + C::RES - 1 + p.window) / C::STR + 1) : n_qt;
+    const int n_steps = max(0, qt_end - qt0);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::BAR_RES_FULL), 1);
@@ -436,7 +439,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             // query columns c < kj - q0 are masked (causal, key after query); only tiles
             // whose first query of this half lies before this warp's last key need it
             const int first_visible = kj - q0;
-            const bool need_mask = p.causal && q0 + c0 < k0 + quarter * 32 + 31;
+            // under a window, query columns c > kj + window - q0 are masked too
+            const int last_visible = p.window >= 0 ? kj + p.window - q0 : C::STR;
+            const bool need_mask = (p.causal && q0 + c0 < k0 + quarter * 32 + 31) ||
+                                   (p.window >= 0 && q0 + c0 + 31 > k0 + quarter * 32 + p.window);
             const uint64_t c2x2 = f32x2(c2, c2);
             const uint64_t zero2 = 0;
             uint32_t rs[32], rd[32], nl[32], nd[32];
@@ -467,7 +473,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (need_mask) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                    if (c0 + e < first_visible) {
+                    if (c0 + e < first_visible || c0 + e > last_visible) {
                         pv[e] = 0.f;
                         dv[e] = 0.f;
                     }
@@ -547,7 +553,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // key tiles this query tile visits (causal: up to its last row's key)
     const int n_kt_all = (p.Lk + C::STR - 1) / C::STR;
     const int last_row = min(q0 + C::RES - 1, p.Lq - 1);
-    const int n_steps = p.causal ? min(min(last_row, p.Lk - 1) / C::STR + 1, n_kt_all) : n_kt_all;
+    const int kt_end = p.causal ? min(min(last_row, p.Lk - 1) / C::STR + 1, n_kt_all) : n_kt_all;
+    // under a sliding window the tile's first row sees nothing left of key q0 - window
+    const int kt0 = p.window >= 0 ? min(max(0, q0 - p.window) / C::STR, kt_end) : 0;
+    const int n_steps = kt_end - kt0;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(C::BAR_RES_FULL), 1);
@@ -595,7 +604,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
-                const int j0 = s * C::STR;
+                const int j0 = (kt0 + s) * C::STR;
                 mbar_arrive_expect_tx(bar(C::BAR_STR_FULL + st), 2 * C::STR_TILE);
 #pragma unroll
                 for (int c = 0; c < C::DB; ++c) {
@@ -705,8 +714,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                             (live ? qi : 0) % BWD_STAT_ROWS;
         const float lse2 = live ? -stat[0] : INFINITY;
         const float dl = live ? -stat[BWD_STAT_ROWS] : 0.f;
-        // keys j < lim are visible to this row
+        // keys lo <= j < lim are visible to this row
         const int lim = p.causal ? min(qi + 1, p.Lk) : p.Lk;
+        const int lo = p.window >= 0 ? qi - p.window : 0;
         // this row of Q (half 0) or of dO (half 1) into TMEM, as a score MMA's A operand
         bool ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
         if (ok) {
@@ -732,10 +742,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t a_s = tmem + lane_base + TM_S + b * C::STR + c0;
             const uint32_t a_dp = tmem + lane_base + TM_DP + b * C::STR + c0;
-            const int j0 = s * C::STR + c0;          // this warp's first key
-            // key columns at or past lim are masked; only a tile reaching lim for some
-            // row of this warp needs the per-element test
-            const bool need_mask = __any_sync(0xffffffffu, j0 + 32 > lim);
+            const int j0 = (kt0 + s) * C::STR + c0;  // this warp's first key
+            // key columns at or past lim (and, under a window, before lo) are masked; only
+            // a tile reaching past those bounds for some row of this warp needs the test
+            const bool need_mask = __any_sync(0xffffffffu, j0 + 32 > lim || j0 < lo);
             // P = 2^(S c - lse2) for this warp's 32 keys, before dP is needed
             float pv[32];
             {
@@ -767,9 +777,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             if (need_mask) {
                 const int hi = lim - j0;             // columns c >= hi are masked
+                const int lo_c = lo - j0;            // and columns c < lo_c
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                    dv[e] = e >= hi ? 0.f : dv[e];
+                    dv[e] = (e >= hi || e < lo_c) ? 0.f : dv[e];
             }
             // dS as bf16 pairs over the first 16 of this warp's 32 columns of the S buffer
             uint32_t dw[16];

@@ -244,6 +244,7 @@ struct BwdArgs {
     void *dq, *dk, *dv;
     int B, H, Lq, Lk, D;
     int causal;
+    int window;               // >= 0 (causal): query i sees keys i - window .. i; -1: none
     float scale;
     int *err;
     unsigned long long wait_limit_ns;

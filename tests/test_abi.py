@@ -32,7 +32,8 @@ def header_functions():
 
 
 def test_header_declares_the_boundary():
-    assert header_functions() == ["fa2_bwd", "fa2_bwd_workspace_size", "fa2_fwd", "fa2_fwd_ex", "fa2_fwd_from_host",
+    assert header_functions() == ["fa2_bwd", "fa2_bwd_window", "fa2_bwd_workspace_size", "fa2_fwd", "fa2_fwd_ex",
+                                  "fa2_fwd_from_host",
                                   "fa2_fwd_noalloc", "fa2_fwd_window", "fa2_fwd_ws", "fa2_get_device_error",
                                   "fa2_status_string", "fa2_version", "fa2_workspace_size"]
 
@@ -163,6 +164,20 @@ def test_bwd_validation(lib):
     assert call_bwd(ws_bytes=4) == INVALID
     assert call_bwd(D=256) == UNSUPPORTED
     assert call_bwd(scale=float("nan")) == INVALID
+
+
+def test_bwd_window_validation(lib):
+    """fa2_bwd_window: a negative window and Lq > Lk are rejected before any CUDA call, and
+    otherwise it checks its arguments as fa2_bwd does."""
+    f = lib.fa2_bwd_window
+
+    def call(Lq=8, Lk=8, D=64, window=4, do=P, ws_bytes=4096):
+        return f(P, P, P, P, P, do, P, P, P, 1, 1, Lq, Lk, D, window, 0.125, P, ws_bytes, None)
+    assert call(window=-1) == INVALID
+    assert call(Lq=9) == INVALID
+    assert call(do=0) == INVALID
+    assert call(ws_bytes=4) == INVALID
+    assert call(D=256) == UNSUPPORTED
 
 
 def test_window_validation(lib):
