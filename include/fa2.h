@@ -275,6 +275,36 @@ fa2_status fa2_bwd_window(const void *q, const void *k, const void *v, const voi
                           void *stream);
 
 /*
+ * fa2_bwd_ex -- the backward pass on strided views, the counterpart of
+ * fa2_fwd_ex: the same computation as fa2_bwd (causal flag) or fa2_bwd_window
+ * (window >= 0, which requires causal and Lq <= Lk), with every [B, H, L, D]
+ * tensor given as a view whose rows of D elements are contiguous.
+ *
+ *   q, k, v, o, dout   bf16 inputs; dq, dk, dv bf16 outputs.  Element
+ *                      (b, h, i, d) of x is at x + b*x_strides[0] +
+ *                      h*x_strides[1] + i*x_strides[2] + d.  A NULL stride
+ *                      array means contiguous [B, H, L, D].  Every stride is in
+ *                      elements, positive, a multiple of 8 (16 bytes) and at
+ *                      most 2^38.  The rows of dq, dk and dv must not overlap
+ *                      one another; the inputs may.
+ *   lse                fp32 [B, H, Lq] contiguous (fa2_fwd_ex's output).
+ *   window             -1: none; w >= 0: as fa2_bwd_window.
+ *   (other arguments and the workspace as fa2_bwd)
+ *
+ * Errors as fa2_bwd, plus FA2_ERR_INVALID_ARG for a stride that breaks the
+ * rules above or a bad window.
+ */
+fa2_status fa2_bwd_ex(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                      int B, int H, int Lq, int Lk, int D,
+                      const long long *q_strides, const long long *k_strides,
+                      const long long *v_strides, const long long *o_strides,
+                      const long long *do_strides, const long long *dq_strides,
+                      const long long *dk_strides, const long long *dv_strides,
+                      int causal, int window, float scale, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
  * fa2_fwd_from_host -- the same pass starting from, and ending in, HOST
  * memory: copies q, k, v from the host into the caller's device staging
  * buffers, runs the pass, and copies O and LSE back into the caller's host

@@ -50,6 +50,8 @@ def load_library() -> ctypes.CDLL:
     lib.fa2_fwd_ex.restype = i
     lib.fa2_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ll3, ll3, ll3, ll3, i, i, f, vp,
                                ctypes.c_size_t, vp]
+    lib.fa2_bwd_ex.restype = i
+    lib.fa2_bwd_ex.argtypes = [vp] * 9 + [i, i, i, i, i] + [ll3] * 8 + [i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa2_fwd_noalloc.restype = i
     lib.fa2_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa2_bwd_workspace_size.restype = i
@@ -191,6 +193,44 @@ def fa2_fwd_ex(q, k, v, o, lse, causal: bool, scale: float | None = None, window
                          ws_ptr, ws_bytes, _stream_handle(stream, q.device))
     if st != 0:
         raise Fa2Error(st, "fa2_fwd_ex")
+
+
+def fa2_bwd_ex(q, k, v, o, lse, do, dq, dk, dv, causal: bool, scale: float | None = None,
+               window: int | None = None, workspace=None, stream=None) -> None:
+    """Backward pass on strided (B, H, L, D) views (fa2_bwd_ex): every tensor but lse may be
+    a view whose last dimension is contiguous and whose other strides are multiples of 8
+    elements; lse is the contiguous (B, H, Lq) output of the forward."""
+    import torch
+    tensors = (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv))
+    if any(t.dim() != 4 for _, t in tensors):
+        raise ValueError("q, k, v, o, do, dq, dk, dv must be 4-D (B, H, L, D) views")
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    for name, t in tensors:
+        want = (B, H, Lk, D) if name in ("k", "v", "dk", "dv") else (B, H, Lq, D)
+        if tuple(t.shape) != want:
+            raise ValueError(f"{name} must have shape {want}, got {tuple(t.shape)}")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if t.stride(3) != 1:
+            raise ValueError(f"{name}'s last dimension must be contiguous")
+        if not t.is_cuda or t.device != q.device:
+            raise ValueError("all tensors must be on the same CUDA device")
+    if tuple(lse.shape) != (B, H, Lq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, Lq) tensor")
+    arrays = [(ctypes.c_longlong * 3)(t.stride(0), t.stride(1), t.stride(2)) for _, t in tensors]
+    if scale is None:
+        scale = D ** -0.5
+    if workspace is None:
+        workspace = torch.empty(max(fa2_bwd_workspace_size(B, H, Lq, Lk, D), 16), dtype=torch.uint8,
+                                device=q.device)
+    st = _lib.fa2_bwd_ex(*(t.data_ptr() for _, t in tensors[:4]), lse.data_ptr(),
+                         *(t.data_ptr() for _, t in tensors[4:]), B, H, Lq, Lk, D, *arrays,
+                         int(bool(causal)), -1 if window is None else int(window), float(scale),
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                         _stream_handle(stream, q.device))
+    if st != 0:
+        raise Fa2Error(st, "fa2_bwd_ex")
 
 
 def fa2_fwd_noalloc(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=None) -> None:

@@ -326,10 +326,26 @@ FA2_EXPORT fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D
 
 namespace fa2 {
 namespace {
+// Zero the rows of a bf16 [B, H, L, D] view (rows of D contiguous) on `stream`.
+bool zero_rows(void *ptr, int B, int H, int L, int D, const BhlStrides &st, cudaStream_t stream)
+{
+    const BhlStrides c = contiguous_bhl(H, L, D);
+    if (st.b == c.b && st.h == c.h && st.l == c.l)
+        return cudaMemsetAsync(ptr, 0, static_cast<size_t>(B) * H * L * D * 2, stream) == cudaSuccess;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            if (cudaMemset2DAsync(static_cast<uint16_t *>(ptr) + b * st.b + h * st.h, static_cast<size_t>(st.l) * 2,
+                                  0, static_cast<size_t>(D) * 2, L, stream) != cudaSuccess)
+                return false;
+    return true;
+}
+
 // The backward pass; window >= 0 (causal only) restricts query i to keys i - window .. i.
+// strides: NULL (everything contiguous) or 8 arrays of (batch, head, row) element strides,
+// for q, k, v, o, dout, dq, dk, dv in that order, each NULL for a contiguous view.
 fa2_status bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
                void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D, int causal, int window, float scale,
-               void *workspace, size_t workspace_bytes, void *stream)
+               void *workspace, size_t workspace_bytes, void *stream, const long long *const *strides = nullptr)
 {
     // the forward's own checks cover q, k, v, o, lse, sizes and scale
     fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
@@ -344,19 +360,39 @@ fa2_status bwd(const void *q, const void *k, const void *v, const void *o, const
         return FA2_ERR_INVALID_ARG;
     if (workspace_bytes < fa2::bwd_stats_bytes(B, H, Lq))
         return FA2_ERR_INVALID_ARG;
+    // q, k, v, o, dout, dq, dk, dv
+    BhlStrides sts[8] = {contiguous_bhl(H, Lq, D), contiguous_bhl(H, Lk, D), contiguous_bhl(H, Lk, D),
+                         contiguous_bhl(H, Lq, D), contiguous_bhl(H, Lq, D), contiguous_bhl(H, Lq, D),
+                         contiguous_bhl(H, Lk, D), contiguous_bhl(H, Lk, D)};
+    for (int i = 0; strides && i < 8; ++i) {
+        if (!strides[i])
+            continue;
+        // positive, and a multiple of 16 bytes (TMA strides; 16-byte row loads and stores)
+        for (int d = 0; d < 3; ++d)
+            if (strides[i][d] <= 0 || strides[i][d] % 8 != 0 || strides[i][d] > (1ll << 38))
+                return FA2_ERR_INVALID_ARG;
+        sts[i] = {strides[i][0], strides[i][1], strides[i][2]};
+    }
     int dev = 0;
     if ((st = fa2::select_device_of(q, &dev)) != FA2_OK)
         return st;
     if (Lq == 0) {   // no queries: every key's gradients are zero
-        const size_t kv_bytes = static_cast<size_t>(B) * H * Lk * D * 2;
-        if (cudaMemsetAsync(dk, 0, kv_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
-            cudaMemsetAsync(dv, 0, kv_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        if (!zero_rows(dk, B, H, Lk, D, sts[6], static_cast<cudaStream_t>(stream)) ||
+            !zero_rows(dv, B, H, Lk, D, sts[7], static_cast<cudaStream_t>(stream))) {
             (void)cudaGetLastError();
             return FA2_ERR_CUDA;
         }
         return FA2_OK;
     }
     fa2::BwdArgs a;
+    a.sq = sts[0];
+    a.sk = sts[1];
+    a.sv = sts[2];
+    a.so = sts[3];
+    a.sdo = sts[4];
+    a.sdq = sts[5];
+    a.sdk = sts[6];
+    a.sdv = sts[7];
     a.q = q;
     a.k = k;
     a.v = v;
@@ -404,6 +440,22 @@ FA2_EXPORT fa2_status fa2_bwd_window(const void *q, const void *k, const void *v
         return FA2_ERR_INVALID_ARG;
     return fa2::bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, D, 1, window, scale, workspace,
                     workspace_bytes, stream);
+}
+
+FA2_EXPORT fa2_status fa2_bwd_ex(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                                 const void *dout, void *dq, void *dk, void *dv, int B, int H, int Lq, int Lk, int D,
+                                 const long long *q_strides, const long long *k_strides, const long long *v_strides,
+                                 const long long *o_strides, const long long *do_strides,
+                                 const long long *dq_strides, const long long *dk_strides,
+                                 const long long *dv_strides, int causal, int window, float scale, void *workspace,
+                                 size_t workspace_bytes, void *stream)
+{
+    if (window < -1 || (window >= 0 && (!causal || Lq > Lk)))
+        return FA2_ERR_INVALID_ARG;
+    const long long *const strides[8] = {q_strides,  k_strides,  v_strides,  o_strides,
+                                         do_strides, dq_strides, dk_strides, dv_strides};
+    return fa2::bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Lq, Lk, D, causal, window, scale, workspace,
+                    workspace_bytes, stream, strides);
 }
 
 FA2_EXPORT fa2_status fa2_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse, int B,

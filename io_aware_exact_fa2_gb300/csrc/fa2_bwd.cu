@@ -33,21 +33,42 @@ static bool set_smem(K kernel, int bytes, int device, std::atomic<unsigned long 
     return true;
 }
 
+// A [B, H, L, D] view as a tensor map with boxes of 64 columns by box_rows rows of one
+// head: 3-D (D, L, B*H) when its batch stride is H times its head stride (or B == 1),
+// else 4-D (D, L, H, B).  Sets *is3 accordingly.
+static bool encode_bwd_map(EncodeTiledFn encode, CUtensorMap *m, const void *ptr, int D, int L, int H, int B,
+                           BhlStrides st, int box_rows, bool *is3)
+{
+    *is3 = B == 1 || st.b == st.h * H;
+    if (!*is3)
+        return encode_bhld_strided(encode, m, ptr, D, L, H, B, st, box_rows);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                          static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(H)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(st.l) * 2, static_cast<cuuint64_t>(st.h) * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 static fa2_status launch_bwd_d(const BwdArgs &a)
 {
     using CKV = BwdKV<D>;
     using CQ = BwdQ<D>;
     const int BH = a.B * a.H;
+    // every input as a tensor map built from its strides (3-D where the heads collapse)
     CUtensorMap q_res, do_res, k_str, v_str, k_res, v_res, q_str, do_str;
-    if (!encode_bhld(a.encode, &q_res, a.q, D, a.Lq, BH, CQ::RES) ||
-        !encode_bhld(a.encode, &do_res, a.dout, D, a.Lq, BH, CQ::RES) ||
-        !encode_bhld(a.encode, &k_str, a.k, D, a.Lk, BH, CQ::STR) ||
-        !encode_bhld(a.encode, &v_str, a.v, D, a.Lk, BH, CQ::STR) ||
-        !encode_bhld(a.encode, &k_res, a.k, D, a.Lk, BH, CKV::RES) ||
-        !encode_bhld(a.encode, &v_res, a.v, D, a.Lk, BH, CKV::RES) ||
-        !encode_bhld(a.encode, &q_str, a.q, D, a.Lq, BH, CKV::STR) ||
-        !encode_bhld(a.encode, &do_str, a.dout, D, a.Lq, BH, CKV::STR))
+    bool q3, k3, v3, do3;
+    if (!encode_bwd_map(a.encode, &q_res, a.q, D, a.Lq, a.H, a.B, a.sq, CQ::RES, &q3) ||
+        !encode_bwd_map(a.encode, &do_res, a.dout, D, a.Lq, a.H, a.B, a.sdo, CQ::RES, &do3) ||
+        !encode_bwd_map(a.encode, &k_str, a.k, D, a.Lk, a.H, a.B, a.sk, CQ::STR, &k3) ||
+        !encode_bwd_map(a.encode, &v_str, a.v, D, a.Lk, a.H, a.B, a.sv, CQ::STR, &v3) ||
+        !encode_bwd_map(a.encode, &k_res, a.k, D, a.Lk, a.H, a.B, a.sk, CKV::RES, &k3) ||
+        !encode_bwd_map(a.encode, &v_res, a.v, D, a.Lk, a.H, a.B, a.sv, CKV::RES, &v3) ||
+        !encode_bwd_map(a.encode, &q_str, a.q, D, a.Lq, a.H, a.B, a.sq, CKV::STR, &q3) ||
+        !encode_bwd_map(a.encode, &do_str, a.dout, D, a.Lq, a.H, a.B, a.sdo, CKV::STR, &do3))
         return FA2_ERR_CUDA;
     BwdParams p;
     const int n_stat_tiles = (a.Lq + BWD_STAT_ROWS - 1) / BWD_STAT_ROWS;
@@ -56,6 +77,18 @@ static fa2_status launch_bwd_d(const BwdArgs &a)
     p.dq = static_cast<uint16_t *>(a.dq);
     p.dk = static_cast<uint16_t *>(a.dk);
     p.dv = static_cast<uint16_t *>(a.dv);
+    p.dq_sb = a.sdq.b;
+    p.dq_sh = a.sdq.h;
+    p.dq_sl = a.sdq.l;
+    p.dk_sb = a.sdk.b;
+    p.dk_sh = a.sdk.h;
+    p.dk_sl = a.sdk.l;
+    p.dv_sb = a.sdv.b;
+    p.dv_sh = a.sdv.h;
+    p.dv_sl = a.sdv.l;
+    p.H = a.H;
+    p.maps3 = (q3 ? 1 << BWD_MAP_Q : 0) | (k3 ? 1 << BWD_MAP_K : 0) | (v3 ? 1 << BWD_MAP_V : 0) |
+              (do3 ? 1 << BWD_MAP_DO : 0);
     p.err = a.err;
     p.wait_limit_ns = a.wait_limit_ns;
     p.Lq = a.Lq;
@@ -75,7 +108,7 @@ static fa2_status launch_bwd_d(const BwdArgs &a)
         constexpr int rpb = bwd_delta_rows_per_block<D>();
         fa2_bwd_delta_kernel<D><<<static_cast<unsigned>((rows + rpb - 1) / rpb), BWD_DELTA_THREADS, 0, a.stream>>>(
             static_cast<const uint16_t *>(a.o), static_cast<const uint16_t *>(a.dout), a.lse, a.stats, a.Lq,
-            n_stat_tiles, rows);
+            n_stat_tiles, rows, a.H, BwdRowStrides{a.so.b, a.so.h, a.so.l}, BwdRowStrides{a.sdo.b, a.sdo.h, a.sdo.l});
         const long long n_qt = (a.Lq + CQ::RES - 1) / CQ::RES;
         fa2_bwd_q_kernel<CQ><<<static_cast<unsigned>(n_qt * BH), CQ::NUM_THREADS, CQ::SMEM_BYTES, a.stream>>>(
             q_res, do_res, k_str, v_str, p);

@@ -148,24 +148,6 @@ inline bool encode_bhld_strided(EncodeTiledFn encode, CUtensorMap *m, const void
     return r == CUDA_SUCCESS;
 }
 
-// 3-D view of a contiguous bf16 [B*H, L, D] tensor: dims (D, L, B*H) innermost
-// first, a box of 64 columns (128 bytes, one swizzle span) by box_rows rows by
-// one head.  Rows outside [0, L) of a head read as zero.
-inline bool encode_bhld(EncodeTiledFn encode, CUtensorMap *m, const void *ptr, int D, int L, int BH,
-                        int box_rows)
-{
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
-                          static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                             static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <class C>
 fa2_status launch_fwd(const LaunchArgs &a)
 {
@@ -245,6 +227,8 @@ struct BwdArgs {
     int B, H, Lq, Lk, D;
     int causal;
     int window;               // >= 0 (causal): query i sees keys i - window .. i; -1: none
+    // element strides (batch, head, row) of every [B, H, L, D] view; rows of D contiguous
+    BhlStrides sq, sk, sv, so, sdo, sdq, sdk, sdv;
     float scale;
     int *err;
     unsigned long long wait_limit_ns;

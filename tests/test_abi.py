@@ -32,7 +32,8 @@ def header_functions():
 
 
 def test_header_declares_the_boundary():
-    assert header_functions() == ["fa2_bwd", "fa2_bwd_window", "fa2_bwd_workspace_size", "fa2_fwd", "fa2_fwd_ex",
+    assert header_functions() == ["fa2_bwd", "fa2_bwd_ex", "fa2_bwd_window", "fa2_bwd_workspace_size", "fa2_fwd",
+                                  "fa2_fwd_ex",
                                   "fa2_fwd_from_host",
                                   "fa2_fwd_noalloc", "fa2_fwd_window", "fa2_fwd_ws", "fa2_get_device_error",
                                   "fa2_status_string", "fa2_version", "fa2_workspace_size"]
@@ -178,6 +179,26 @@ def test_bwd_window_validation(lib):
     assert call(do=0) == INVALID
     assert call(ws_bytes=4) == INVALID
     assert call(D=256) == UNSUPPORTED
+
+
+def test_bwd_ex_validation(lib):
+    """fa2_bwd_ex rejects strides that are not positive multiples of 8 elements (or above
+    2^38) and a bad window, before any CUDA call."""
+    f = lib.fa2_bwd_ex
+    ll3 = ctypes.c_longlong * 3
+
+    def call(bad=None, at=0, causal=1, window=-1, Lq=8, Lk=8):
+        arrays = [None] * 8
+        if bad is not None:
+            arrays[at] = ll3(*bad)
+        return f(P, P, P, P, P, P, P, P, P, 1, 1, Lq, Lk, 64, *arrays, causal, window, 0.125, P, 4096, None)
+    for at in range(8):
+        assert call((8 * 64, 64, 68), at) == INVALID     # row stride not a multiple of 8
+        assert call((8 * 64, 0, 64), at) == INVALID      # zero head stride
+        assert call((1 << 39, 512, 64), at) == INVALID   # beyond 2^38
+    assert call(window=-2) == INVALID
+    assert call(window=4, causal=0) == INVALID
+    assert call(window=4, Lq=9) == INVALID
 
 
 def test_window_validation(lib):

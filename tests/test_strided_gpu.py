@@ -118,3 +118,99 @@ def test_rejects_unaligned_strides():
     lse = torch.empty(B, H, L, dtype=torch.float32, device=DEV)
     with pytest.raises(Fa2Error):
         fa2_fwd_ex(q, q, q, o, lse, False)
+
+
+# ---------------------------------------------------------------- backward (fa2_bwd_ex)
+def _contiguous_bwd(q, k, v, do, causal, scale, window=None):
+    """Forward and backward on contiguous copies: (o, lse, dq, dk, dv)."""
+    from io_aware_exact_fa2_gb300 import fa2_bwd, fa2_bwd_window
+    qc, kc, vc, dc = (t.contiguous() for t in (q, k, v, do))
+    o, lse = _contiguous_run(qc, kc, vc, causal, scale, window)
+    grads = [torch.full_like(t, float("nan")) for t in (qc, kc, vc)]
+    if window is None:
+        fa2_bwd(qc, kc, vc, o, lse, dc, *grads, causal, scale)
+    else:
+        fa2_bwd_window(qc, kc, vc, o, lse, dc, *grads, window, scale)
+    return (o, lse, *grads)
+
+
+def _strided_bwd(q, k, v, do, o, lse, grads, causal, scale, window=None):
+    from io_aware_exact_fa2_gb300 import fa2_bwd_ex, fa2_get_device_error
+    for g in grads:
+        g.fill_(float("nan"))
+    fa2_bwd_ex(q, k, v, o, lse, do, *grads, causal, scale, window=window)
+    st, code = fa2_get_device_error()
+    assert st == 0, f"device error {st} code {code:#x}"
+    return grads
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+def test_bwd_blhd_views_match_contiguous(D, causal):
+    """Every tensor of the backward stored as [B, L, H, D] and viewed as [B, H, L, D]:
+    bit-identical to fa2_bwd on contiguous copies."""
+    B, H, Lq, Lk = 2, 3, 300, 457 if not causal else 300
+    q, k, v = (t.to(DEV) for t in make_qkv(B, H, Lq, Lk, D, seed_base=9600 + D))
+    do = make_qkv(B, H, Lq, Lq, D, seed_base=9650 + D)[0].to(DEV)
+    scale = D ** -0.5
+    o, lse, *ref = _contiguous_bwd(q, k, v, do, causal, scale)
+    grads = [torch.empty(B, L, H, D, dtype=torch.bfloat16, device=DEV).transpose(1, 2) for L in (Lq, Lk, Lk)]
+    got = _strided_bwd(_blhd(q), _blhd(k), _blhd(v), _blhd(do), _blhd(o), lse, grads, causal, scale)
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
+def test_bwd_packed_qkv_and_packed_gradients(causal):
+    """q, k, v as slices of one packed [B, L, 3, H, D] tensor and dq, dk, dv written into the
+    slices of one packed gradient tensor of the same layout; bit-identical to the contiguous
+    backward, and checked against the oracle's gradients."""
+    B, H, L, D = 1, 4, 389, 128
+    qh, kh, vh = make_qkv(B, H, L, L, D, seed_base=9700)
+    doh = make_qkv(B, H, L, L, D, seed_base=9750)[0]
+    packed = torch.stack([t.transpose(1, 2) for t in (qh, kh, vh)], dim=2).contiguous().to(DEV)
+    q, k, v = (packed[:, :, i].transpose(1, 2) for i in range(3))
+    do = doh.to(DEV)
+    scale = D ** -0.5
+    o, lse, *ref = _contiguous_bwd(q, k, v, do, causal, scale)
+    gpacked = torch.empty(B, L, 3, H, D, dtype=torch.bfloat16, device=DEV)
+    grads = [gpacked[:, :, i].transpose(1, 2) for i in range(3)]
+    got = _strided_bwd(q, k, v, do, o, lse, grads, causal, scale)
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
+    from test_bwd_gpu import compare_grads
+    compare_grads((qh, kh, vh, doh, scale), [g.contiguous().cpu() for g in got], causal)
+
+
+def test_bwd_window_with_strided_views():
+    B, H, L, D, w = 1, 2, 700, 64, 100
+    q, k, v = (t.to(DEV) for t in make_qkv(B, H, L, L, D, seed_base=9800))
+    do = make_qkv(B, H, L, L, D, seed_base=9850)[0].to(DEV)
+    o, lse, *ref = _contiguous_bwd(q, k, v, do, True, D ** -0.5, window=w)
+    grads = [torch.empty(B, L, H, D, dtype=torch.bfloat16, device=DEV).transpose(1, 2) for _ in range(3)]
+    got = _strided_bwd(_blhd(q), _blhd(k), _blhd(v), _blhd(do), _blhd(o), lse, grads, True, D ** -0.5, window=w)
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
+
+
+def test_bwd_no_queries_zeroes_strided_key_gradients():
+    """Lq = 0: dk and dv are zeroed row by row in their strided views, and nothing else moves
+    (the query-side buffers are never read; dummies stand in for the empty tensors)."""
+    import ctypes
+    from io_aware_exact_fa2_gb300 import _binding
+    B, H, Lk, D = 2, 3, 50, 64
+    k = torch.randn(B, H, Lk, D, device=DEV).to(torch.bfloat16)
+    dummy = torch.zeros(64, dtype=torch.bfloat16, device=DEV)
+    lse = torch.zeros(4, dtype=torch.float32, device=DEV)
+    wide = torch.full((B, Lk, H, 2 * D), 7.0, dtype=torch.bfloat16, device=DEV)
+    dk = wide[..., :D].transpose(1, 2)           # rows 2*D elements apart; the other half must stay 7
+    dv = torch.full((B, H, Lk, D), 7.0, dtype=torch.bfloat16, device=DEV)
+    ll3 = ctypes.c_longlong * 3
+    strides = [None] * 6 + [ll3(dk.stride(0), dk.stride(1), dk.stride(2)), None]
+    p = dummy.data_ptr()
+    st = _binding._lib.fa2_bwd_ex(p, k.data_ptr(), k.data_ptr(), p, lse.data_ptr(), p, p, dk.data_ptr(),
+                                  dv.data_ptr(), B, H, 0, Lk, D, *strides, 0, -1, 0.125, None, 0, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+    assert bool((wide[..., D:] == 7.0).all())
