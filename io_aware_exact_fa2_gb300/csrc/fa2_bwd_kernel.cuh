@@ -269,10 +269,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
-    // key tiles in order (heaviest first when causal: low keys are seen by the most queries)
+    // Causal: key tiles in order across heads, heaviest first (low keys are seen by the
+    // most queries).  Otherwise head by head, so the CTAs running at one time stream the
+    // same few heads' Q and dO through L2.
     const int n_kt = (p.Lk + C::RES - 1) / C::RES;
-    const int kt = static_cast<int>(blockIdx.x) / p.BH;
-    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    const int kt = p.causal ? static_cast<int>(blockIdx.x) / p.BH : static_cast<int>(blockIdx.x) % n_kt;
+    const int bh = p.causal ? static_cast<int>(blockIdx.x) % p.BH : static_cast<int>(blockIdx.x) / n_kt;
     if (kt >= n_kt)
         return;
     const int hh = bh % p.H, hb = bh / p.H;   // head and batch of this CTA's tiles
@@ -576,10 +578,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
-    // query tiles, last (heaviest when causal) first
+    // Causal: query tiles across heads, last (heaviest) first.  Otherwise head by head,
+    // so the CTAs running at one time stream the same few heads' K and V through L2.
     const int n_qt = (p.Lq + C::RES - 1) / C::RES;
-    const int qt = n_qt - 1 - static_cast<int>(blockIdx.x) / p.BH;
-    const int bh = static_cast<int>(blockIdx.x) % p.BH;
+    const int qt = p.causal ? n_qt - 1 - static_cast<int>(blockIdx.x) / p.BH : static_cast<int>(blockIdx.x) % n_qt;
+    const int bh = p.causal ? static_cast<int>(blockIdx.x) % p.BH : static_cast<int>(blockIdx.x) / n_qt;
     if (qt < 0)
         return;
     const int hh = bh % p.H, hb = bh / p.H;   // head and batch of this CTA's tiles
