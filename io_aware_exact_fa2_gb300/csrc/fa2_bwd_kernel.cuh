@@ -51,6 +51,7 @@ struct BwdParams {
     uint16_t *dk, *dv;      // bf16 [B, H, Lk, D] views, likewise
     long long dq_sb, dq_sh, dq_sl, dk_sb, dk_sh, dk_sl, dv_sb, dv_sh, dv_sl;   // element strides
     int H;                  // heads: flat head bh = b * H + h
+    int head_group;         // causal grids: heads per group (heaviest tiles first within a group)
     // bit m set: tensor map m (BWD_MAP_*) is 3-D (D, L, B*H), else 4-D (D, L, H, B)
     int maps3;
     int *err;
@@ -245,6 +246,22 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, float mul, uint16_
     }
 }
 
+// CTA idx of a gradient grid (n_tiles resident tiles per head, all heads) -> (tile, head).
+// Causal grids go group by group (head_group heads each) and, within a group, tile by
+// tile across its heads; other grids go head by head.
+__device__ __forceinline__ void bwd_cta_tile(int idx, int n_tiles, const BwdParams &p, int &tile, int &bh)
+{
+    if (!p.causal) {
+        tile = idx % n_tiles;
+        bh = idx / n_tiles;
+        return;
+    }
+    const int grp = idx / (p.head_group * n_tiles), rem = idx % (p.head_group * n_tiles);
+    const int g0 = grp * p.head_group, gn = min(p.head_group, p.BH - g0);
+    tile = rem / gn;
+    bh = g0 + rem % gn;
+}
+
 // ============================================================== dK, dV kernel
 // CTA = one tile of RES = 128 keys of one (b, h); steps = query tiles of STR rows.
 // TMEM: dV (D cols), dK (D cols), two S^T buffers and two dP^T buffers (STR cols
@@ -269,12 +286,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
-    // Causal: key tiles in order across heads, heaviest first (low keys are seen by the
-    // most queries).  Otherwise head by head, so the CTAs running at one time stream the
-    // same few heads' Q and dO through L2.
+    // Causal: groups of head_group heads whose streamed Q and dO fit in L2 together; within
+    // a group, key tiles in order across its heads, heaviest first (low keys are seen by
+    // the most queries).  Otherwise head by head, so the CTAs running at one time stream
+    // the same few heads' Q and dO through L2.
     const int n_kt = (p.Lk + C::RES - 1) / C::RES;
-    const int kt = p.causal ? static_cast<int>(blockIdx.x) / p.BH : static_cast<int>(blockIdx.x) % n_kt;
-    const int bh = p.causal ? static_cast<int>(blockIdx.x) % p.BH : static_cast<int>(blockIdx.x) / n_kt;
+    int kt, bh;
+    bwd_cta_tile(static_cast<int>(blockIdx.x), n_kt, p, kt, bh);
     if (kt >= n_kt)
         return;
     const int hh = bh % p.H, hb = bh / p.H;   // head and batch of this CTA's tiles
@@ -578,11 +596,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
-    // Causal: query tiles across heads, last (heaviest) first.  Otherwise head by head,
-    // so the CTAs running at one time stream the same few heads' K and V through L2.
+    // Causal: groups of head_group heads, within a group query tiles across its heads,
+    // last (heaviest) first.  Otherwise head by head, so the CTAs running at one time
+    // stream the same few heads' K and V through L2.
     const int n_qt = (p.Lq + C::RES - 1) / C::RES;
-    const int qt = p.causal ? n_qt - 1 - static_cast<int>(blockIdx.x) / p.BH : static_cast<int>(blockIdx.x) % n_qt;
-    const int bh = p.causal ? static_cast<int>(blockIdx.x) % p.BH : static_cast<int>(blockIdx.x) / n_qt;
+    int qt, bh;
+    bwd_cta_tile(static_cast<int>(blockIdx.x), n_qt, p, qt, bh);
+    if (p.causal)
+        qt = n_qt - 1 - qt;
     if (qt < 0)
         return;
     const int hh = bh % p.H, hb = bh / p.H;   // head and batch of this CTA's tiles
