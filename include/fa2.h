@@ -36,6 +36,10 @@
  *   - Re-entrant and thread-safe; the library keeps no per-call state (but
  *     calls of fa2_fwd_noalloc that overlap on the GPU share its scratch).
  *   - O and LSE rows i >= Lq are never written; inputs are never written.
+ *   - Per device, the library looks up the device addresses of its own
+ *     globals (the error word, fa2_fwd_noalloc's scratch) once and keeps them
+ *     for the life of the process.  Tearing the device's context down between
+ *     calls (cudaDeviceReset) is not supported.
  */
 #ifndef FA2_GB300_H
 #define FA2_GB300_H
@@ -217,6 +221,41 @@ fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o,
                            int causal, float scale, void *stream);
 
 /*
+ * fa2_fwd_fp8 -- the forward pass on e4m3 inputs: the FP8 mode of
+ * FlashAttention-3 that "Flash Attention: principles and implementation"
+ * (tbr8.org), section 4.3, names.  The page fixes no format; this library's
+ * reading: Q, K and V are stored as e4m3 (OCP FP8 E4M3: bias 7, largest finite
+ * 448, no infinities) with one fp32 descale per (batch, head) each, the real
+ * input being the stored value times its descale.  The pass computes
+ *
+ *     s_ij = scale * dq[b,h] * dk[b,h] * sum_d Q8[b,h,i,d] * K8[b,h,j,d]
+ *     O[b,h,i,:] = dv[b,h] * sum_j P~_ij V8[b,h,j,:] / sum_j P~_ij
+ *     LSE[b,h,i] = ln sum_j exp(s_ij)                       (natural log)
+ *
+ * where the products accumulate in fp32 on the tensor cores (kind::f8f6f4)
+ * and P~ are the softmax weights (relative to the running row max, at most
+ * 2^8) rounded to e4m3 for the P V product; O is divided by the sum of those
+ * rounded weights and LSE comes from the unrounded fp32 sum.
+ *
+ *   q, k, v     device pointers, e4m3 bytes [B, H, Lq|Lk, D], contiguous.
+ *   descale_q, descale_k, descale_v
+ *               device pointers, fp32 [B, H] (4-byte aligned), read only.
+ *   o, lse      as fa2_fwd (bf16 O, fp32 natural-log LSE of the real scores).
+ *   D           must be 128.
+ *   workspace, workspace_bytes
+ *               optional, as fa2_fwd_ws; the size is fa2_workspace_size() of
+ *               the same problem with D = 128 (NULL: whole query tiles).
+ *
+ * Errors: as fa2_fwd_ws; FA2_ERR_INVALID_ARG also for a missing or misaligned
+ * descale pointer; FA2_ERR_UNSUPPORTED for D != 128.
+ */
+fa2_status fa2_fwd_fp8(const void *q, const void *k, const void *v,
+                       const float *descale_q, const float *descale_k,
+                       const float *descale_v, void *o, float *lse, int B,
+                       int H, int Lq, int Lk, int D, int causal, float scale,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * fa2_bwd_workspace_size -- bytes of device workspace fa2_bwd needs: two fp32
  * per query row (-lse * log2 e and -Delta), rows padded to a multiple of 64
  * per head.  Returns FA2_OK; FA2_ERR_INVALID_ARG for bad sizes;
@@ -334,11 +373,31 @@ fa2_status fa2_fwd_from_host(const void *q_host, const void *k_host,
 /*
  * fa2_get_device_error -- synchronises `stream`, then reads and clears the
  * library's device-side error word on the current device.  Every inter-warp
- * wait inside the kernels is bounded (about one second); a wait that runs out
- * records a code here, the kernel winds down without hanging the GPU, and
- * its outputs are undefined.
+ * wait inside the kernels is bounded (one second; FA2_WAIT_LIMIT_MS in the
+ * environment changes it); a wait that runs out records a code here, the
+ * kernel winds down without hanging the GPU (each CTA first waits for the
+ * copies and MMAs it has issued), and the outputs of that call are undefined
+ * (a workspace it used must be zero-filled again before reuse).
  *
- *   detail   optional (may be NULL): receives the raw code (0 = none).
+ * The word is one per device, shared by every stream and every call of this
+ * library on that device: the first fa2_get_device_error to read it after a
+ * time-out reports and clears it, whichever stream that call names.  `stream`
+ * only selects what is synchronised before the read, so to attribute a
+ * time-out to one stream's calls, read the word with every other stream of
+ * this library idle.
+ *
+ * For tests only, two environment variables (read on every call) exercise
+ * this path in the forward kernel: FA2_TEST_STALL=1 makes its softmax warps
+ * first wait on a barrier nothing completes (that wait runs out, then the
+ * other roles' waits on them), and FA2_TEST_WAIT_LIMIT_NS (nanoseconds)
+ * shortens its inter-warp waits so the test ends quickly; the waits for a
+ * CTA's own copies and MMAs keep the full bound.
+ *
+ *   detail   optional (may be NULL): receives the raw code (0 = none): the
+ *            waiting role in bits 8-11 (forward: 1 TMA producer, 2 MMA
+ *            issuer, 3 softmax, 4 a CTA's final wait for its own work;
+ *            backward: 5 producer, 6 MMA issuer, 7 elementwise warps) and the
+ *            barrier in the low byte.
  *
  * Returns FA2_OK, FA2_ERR_TIMEOUT, or FA2_ERR_CUDA if the synchronisation or
  * the read fails.

@@ -12,7 +12,7 @@ a machine without a GPU.
 from . import workloads  # noqa: F401
 
 _BINDING_NAMES = (
-    "fa2_fwd", "fa2_fwd_from_host", "fa2_get_device_error", "fa2_status_string",
+    "fa2_fwd", "fa2_fwd_fp8", "fa2_fwd_from_host", "fa2_get_device_error", "fa2_status_string",
     "fa2_workspace_size", "fa2_workspace", "fa2_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "fa2_bwd", "fa2_bwd_window", "fa2_bwd_ex", "fa2_bwd_workspace_size", "fa2_fwd_window", "fa2_fwd_ex",
     "fa2_version", "Fa2Error", "library_path", "load_library", "STATUS",

@@ -52,6 +52,8 @@ def load_library() -> ctypes.CDLL:
                                ctypes.c_size_t, vp]
     lib.fa2_bwd_ex.restype = i
     lib.fa2_bwd_ex.argtypes = [vp] * 9 + [i, i, i, i, i] + [ll3] * 8 + [i, i, f, vp, ctypes.c_size_t, vp]
+    lib.fa2_fwd_fp8.restype = i
+    lib.fa2_fwd_fp8.argtypes = [vp] * 8 + [i, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.fa2_fwd_noalloc.restype = i
     lib.fa2_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.fa2_bwd_workspace_size.restype = i
@@ -141,6 +143,44 @@ def fa2_fwd(q, k, v, o, lse, causal: bool, scale: float | None = None, stream=No
         where = "fa2_fwd_ws"
     if st != 0:
         raise Fa2Error(st, where)
+
+
+def fa2_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, o, lse, causal: bool, scale: float | None = None,
+                stream=None, workspace=None) -> None:
+    """Forward pass on e4m3 inputs (fa2_fwd_fp8): q8 (B, H, Lq, 128), k8 and v8 (B, H, Lk, 128)
+    float8_e4m3fn CUDA tensors, each with a float32 (B, H) CUDA tensor of descales (the real
+    input is the stored value times its head's descale).  Writes o (bf16) and lse (fp32).
+    `workspace` as for fa2_fwd (fa2_workspace on a D = 128 problem of the same shape)."""
+    import torch
+    if q8.dim() != 4 or k8.dim() != 4 or v8.dim() != 4:
+        raise ValueError("q8, k8, v8 must be 4-D (B, H, L, D)")
+    B, H, Lq, D = q8.shape
+    Lk = k8.shape[2]
+    if tuple(k8.shape) != (B, H, Lk, D) or tuple(v8.shape) != (B, H, Lk, D):
+        raise ValueError(f"shape mismatch: q {tuple(q8.shape)} k {tuple(k8.shape)} v {tuple(v8.shape)}")
+    if tuple(o.shape) != (B, H, Lq, D) or tuple(lse.shape) != (B, H, Lq):
+        raise ValueError("o must be (B, H, Lq, D) and lse (B, H, Lq)")
+    for name, t, dt in (("q8", q8, torch.float8_e4m3fn), ("k8", k8, torch.float8_e4m3fn),
+                        ("v8", v8, torch.float8_e4m3fn), ("o", o, torch.bfloat16), ("lse", lse, torch.float32),
+                        ("descale_q", descale_q, torch.float32), ("descale_k", descale_k, torch.float32),
+                        ("descale_v", descale_v, torch.float32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous() or not t.is_cuda or t.device != q8.device:
+            raise ValueError(f"{name} must be contiguous and on q8's CUDA device")
+    for name, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+        if t.numel() != B * H:
+            raise ValueError(f"{name} must hold one value per (batch, head)")
+    if scale is None:
+        scale = D ** -0.5
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = _lib.fa2_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), descale_q.data_ptr(), descale_k.data_ptr(),
+                          descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Lq, Lk, D, int(bool(causal)),
+                          float(scale), ws_ptr, ws_bytes, _stream_handle(stream, q8.device))
+    if st != 0:
+        raise Fa2Error(st, "fa2_fwd_fp8")
 
 
 def fa2_fwd_window(q, k, v, o, lse, window: int, scale: float | None = None, stream=None) -> None:

@@ -24,7 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libfa2_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["fa2_api.cu", "fa2_noalloc.cu", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu", "fa2_fwd_d256.cu", "fa2_bwd.cu"]
+SOURCES = ["fa2_api.cu", "fa2_noalloc.cu", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu", "fa2_fwd_d256.cu",
+           "fa2_fwd_fp8_d128.cu", "fa2_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC,-fvisibility=hidden", "-Xptxas", "-v",
@@ -58,7 +59,7 @@ def kernel_digest() -> str:
     h = hashlib.sha256()
     files = sorted(f for f in os.listdir(CSRC)
                    if f in ("fa2_fwd_kernel.cuh", "sm103_ptx.cuh", "fa2_launch.cuh", "fa2_split_ranges.h")
-                   or (f.startswith("fa2_fwd_d") and f.endswith(".cu")))
+                   or (f.startswith("fa2_fwd_") and f.endswith(".cu")))
     for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())

@@ -58,6 +58,27 @@ unsigned long long wait_limit_ns()
     return limit;
 }
 
+// Limit of the forward kernel's waits between its warps.  FA2_TEST_WAIT_LIMIT_NS
+// (read on every call, nanoseconds) shortens it so that a test of the time-out path
+// ends quickly; the waits with which a CTA drains its own copies and MMAs before
+// exiting keep the full limit.
+unsigned long long fwd_wait_limit_ns()
+{
+    const char *s = std::getenv("FA2_TEST_WAIT_LIMIT_NS");
+    const long long ns = s ? std::atoll(s) : 0;
+    return ns > 0 ? static_cast<unsigned long long>(ns) : wait_limit_ns();
+}
+
+// Tests of the time-out path: FA2_TEST_STALL=1 (read on every call) makes the forward
+// kernel's softmax warps first wait on a barrier nothing completes, so that wait runs
+// out, the waits of the other roles on those warps run out after it, and the call
+// reports FA2_ERR_TIMEOUT.
+int fwd_stall_test()
+{
+    const char *s = std::getenv("FA2_TEST_STALL");
+    return s && std::strcmp(s, "1") == 0 ? 1 : 0;
+}
+
 // Whether non-causal passes given a workspace cut their key-tile iterations
 // into equal per-SM ranges: FA2_SPLIT=always / never overrides the cost model
 // (read on every call, so a process can switch it between calls).
@@ -187,7 +208,8 @@ fa2_status select_device_of(const void *ptr, int *dev_out)
 
 fa2_status launch(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Lq,
                   int Lk, int D, int causal, float scale, cudaStream_t stream, void *workspace = nullptr,
-                  size_t workspace_bytes = 0, int window = -1, const BhlStrides *strides = nullptr)
+                  size_t workspace_bytes = 0, int window = -1, const BhlStrides *strides = nullptr,
+                  const float *const *descales = nullptr)
 {
     int dev = 0;
     fa2_status st = select_device_of(q, &dev);
@@ -212,7 +234,9 @@ fa2_status launch(const void *q, const void *k, const void *v, void *o, float *l
     a.window = window;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * kLog2e);
     a.err = device_error_ptr(dev);
-    a.wait_limit_ns = wait_limit_ns();
+    a.wait_limit_ns = fwd_wait_limit_ns();
+    a.drain_limit_ns = wait_limit_ns();
+    a.stall_test = fwd_stall_test();
     a.stream = stream;
     a.encode = encode_fn();
     a.device = dev;
@@ -222,6 +246,12 @@ fa2_status launch(const void *q, const void *k, const void *v, void *o, float *l
     a.workspace_bytes = workspace_bytes;
     if (!a.err || !a.encode || a.num_sms <= 0)
         return FA2_ERR_CUDA;
+    if (descales) {   // e4m3 inputs
+        a.descale_q = descales[0];
+        a.descale_k = descales[1];
+        a.descale_v = descales[2];
+        return D == 128 ? launch_fwd_fp8_d128(a) : FA2_ERR_UNSUPPORTED;
+    }
     switch (D) {
     case 64: return launch_fwd_d64(a);
     case 128: return launch_fwd_d128(a);
@@ -277,6 +307,30 @@ FA2_EXPORT fa2_status fa2_fwd_ws(const void *q, const void *k, const void *v, vo
         return FA2_ERR_INVALID_ARG;
     return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, static_cast<cudaStream_t>(stream),
                        workspace, workspace_bytes);
+}
+
+FA2_EXPORT fa2_status fa2_fwd_fp8(const void *q, const void *k, const void *v, const float *descale_q,
+                                  const float *descale_k, const float *descale_v, void *o, float *lse, int B, int H,
+                                  int Lq, int Lk, int D, int causal, float scale, void *workspace,
+                                  size_t workspace_bytes, void *stream)
+{
+    fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
+    if (st != FA2_OK)
+        return st;
+    if (!descale_q || !descale_k || !descale_v || !fa2::aligned(descale_q, 4) || !fa2::aligned(descale_k, 4) ||
+        !fa2::aligned(descale_v, 4))
+        return FA2_ERR_INVALID_ARG;
+    if (D != 128)
+        return FA2_ERR_UNSUPPORTED;
+    if (Lq == 0)
+        return FA2_OK;
+    if (workspace && !fa2::aligned(workspace, 256))
+        return FA2_ERR_INVALID_ARG;
+    const float *ds[3] = {descale_q, descale_k, descale_v};
+    // the e4m3 configuration cuts and merges like the bf16 one at D = 128 (same query and
+    // key tiles), so fa2_workspace_size(..., D = 128, ...) sizes its workspace
+    return fa2::launch(q, k, v, o, lse, B, H, Lq, Lk, D, causal, scale, static_cast<cudaStream_t>(stream),
+                       causal ? nullptr : workspace, causal ? 0 : workspace_bytes, -1, nullptr, ds);
 }
 
 FA2_EXPORT fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse, int B,

@@ -11,7 +11,7 @@
 namespace fa2 {
 
 // Tile configuration (K/V rows, Q tiles per CTA, ring stages, warps per row,
-// S buffers per Q tile, Q kept in TMEM);
+// S buffers per Q tile, Q kept in TMEM, P in two terms);
 // overridable at compile time for tuning sweeps.
 #ifndef FA2_D256_BN
 #define FA2_D256_BN 64
@@ -31,9 +31,14 @@ namespace fa2 {
 #ifndef FA2_D256_CS
 #define FA2_D256_CS 1
 #endif
+// P as two bf16 terms (weight and residual): keeps O within the bf16 output's own
+// rounding where two or three keys dominate a row, at the price of a second PV MMA
+#ifndef FA2_D256_P2
+#define FA2_D256_P2 (FA2_D256_CS == 1)
+#endif
 
 using CfgD256 = FwdCfg<256, FA2_D256_BN, FA2_D256_NQ, FA2_D256_KS, FA2_D256_CS, FA2_D256_NS,
-                      FA2_D256_QT>;
+                      FA2_D256_QT, FA2_D256_P2>;
 
 fa2_status launch_fwd_d256(const LaunchArgs &a) { return launch_fwd<CfgD256>(a); }
 

@@ -40,8 +40,9 @@
 //     row's max grows by more than 2^8 (the stale max is kept otherwise, which
 //     is exact because l and LSE use the same max).
 //   * Epilogue: the softmax warps read O out of TMEM, release it to the MMA
-//     warp (the next unit's PV may then overwrite it), multiply by 1/l and
-//     store bf16 rows and the fp32 LSE straight to global memory.
+//     warp (the next unit's PV may then overwrite it), multiply by 1/l, stage
+//     bf16 blocks of 32 rows x 64 columns in shared memory and write each with
+//     one TMA store (whole 128-byte lines); the fp32 LSE goes straight out.
 //   * Every wait between warps is on an mbarrier with a time bound; a wait
 //     that runs out records a code in a device error word and the CTA winds
 //     down, so no input can hang the GPU.
@@ -57,12 +58,14 @@
 namespace fa2 {
 
 struct FwdParams {
-    uint16_t *o;                // bf16 rows of D (row (b, h, i) at b*o_sb + h*o_sh + i*o_sl)
-    long long o_sb, o_sh, o_sl; // O element strides of b, h and the row
-    float *lse;                 // fp32 [B*H, Lq]
+    float *lse;                 // fp32 [B*H, Lq] (O is written through its tensor map)
+    // e4m3 inputs only: fp32 [B*H] descales of Q, K and V (real input = stored value x descale)
+    const float *descale_q, *descale_k, *descale_v;
     int H;                      // heads (Q/K/V tensor maps are (D, L, H, B))
     int *err;                   // device error word
-    unsigned long long wait_limit_ns;
+    unsigned long long wait_limit_ns;    // bound of every wait between warps
+    int stall_test;             // tests only: the softmax warps first wait on a barrier nobody completes
+    unsigned long long drain_limit_ns;   // bound of a CTA's waits for its own copies / MMAs before exit
     int Lq, Lk;
     int BH;                     // B * H
     int n_qgroups;              // ceil(Lq / (NQ * 128))
@@ -99,11 +102,18 @@ enum : int {
     ERR_DRAIN = 0x400,
 };
 
+// Exponentials taken on the FMA pipe (exp2_poly_f32x2) instead of the MUFU: pairs
+// per 32 columns of a row's scores (0: all on the MUFU).
+#ifndef FA2_EXP2_EMU_PAIRS
+#define FA2_EXP2_EMU_PAIRS 0
+#endif
+
 // Threshold (log2 units) above which a growing row max forces a rescale of O and l.
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.69314718055994530942f;
 
-template <int D_, int BN_, int NQ_, int KS_, int CS_, int NS_ = (NQ_ == 1 ? 2 : 1), int QT_ = 0>
+template <int D_, int BN_, int NQ_, int KS_, int CS_, int NS_ = (NQ_ == 1 ? 2 : 1), int QT_ = 0, int P2_ = 0,
+          int F8_ = 0>
 struct FwdCfg {
     static constexpr int D = D_;     // head dimension
     static constexpr int BN = BN_;   // K/V rows per tile
@@ -115,6 +125,18 @@ struct FwdCfg {
     // QT: Q lives in TMEM and S = Q K^T takes A from TMEM; the softmax warps copy each
     // Q tile there from shared memory.  Needs one Q tile per unit (TMEM budget).
     static constexpr bool QT = QT_ != 0;
+    // P2: P goes to the PV MMA as two bf16 terms, p_hi = bf16(p) and the residual
+    // p_lo = bf16(p - p_hi), over the two halves of the S buffer; O then weighs V
+    // with p to about 2^-17 of itself (one bf16 term rounds each weight by up to
+    // 2^-9), at the price of a second PV MMA per key tile.
+    static constexpr bool P2 = P2_ != 0;
+    // F8: Q, K, V and P are e4m3 bytes and both products run as kind::f8f6f4 MMAs (K
+    // steps of 32 elements); the real inputs are the stored values times per-(batch,
+    // head) descales, folded into the score scale (Q, K) and into O's 1/l (V)
+    static constexpr bool F8 = F8_ != 0;
+    static constexpr int EB = F8 ? 1 : 2;             // bytes per Q/K/V element
+    static constexpr int ECOLS = 128 / EB;             // elements per 128-byte swizzle span
+    static constexpr int KSTEP = 32 / EB;              // elements per MMA K step (32 bytes)
     // NP: P is handed to the MMA warp in NP key parts, so PV on the earlier parts
     // runs while the softmax computes the later ones (one warp per row only: with a
     // column split, a slice's parts are not contiguous key ranges)
@@ -125,7 +147,11 @@ struct FwdCfg {
     static_assert(NP == 1 || NP == 2 || NP == 4, "P goes over in 1, 2 or 4 parts");
     static constexpr int NCOL = BN / CS;          // S columns per softmax thread
     static constexpr int OCOL = D / CS;           // O columns per softmax thread
-    static constexpr int DB = D / 64;             // 64-column (128-byte) swizzle blocks
+    static constexpr int DB = D / ECOLS;          // 128-byte swizzle blocks per row
+    static constexpr int S_KSTEPS = D / KSTEP;    // K steps of S = Q K^T
+    static constexpr int PV_KSTEPS = BN / KSTEP;  // K steps of O += P V
+    static constexpr int PV_KSTEP_BYTES = KSTEP * 128;   // V rows of one K step (MN-major operand)
+    static constexpr int PW = NCOL * EB / 4;      // 32-bit TMEM columns of one thread's slice of P
     static constexpr int Q_BLOCK = BM * 128;
     static constexpr int KV_BLOCK = BN * 128;
     static constexpr int Q_TILE = DB * Q_BLOCK;
@@ -135,9 +161,15 @@ struct FwdCfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
-    static constexpr int OFF_XMAX = OFF_V + KS * KV_TILE;           // f32 [NQ][2][CS][128]
-    static constexpr int OFF_XL = OFF_XMAX + NQ * 2 * CS * 128 * 4;  // f32x2 [NQ][CS][128]
-    static constexpr int OFF_FLAG = OFF_XL + NQ * CS * 128 * 8;       // u32 [NQ] (+ pad)
+    // O staging of the epilogue: each softmax warp's 32 rows x OBW columns of bf16
+    // (64 columns, 128B-swizzled; 32 columns, 64B-swizzled, when a warp owns only 32
+    // columns of a row), the shared-memory side of one TMA store box
+    static constexpr int OBW = (D / CS) >= 64 ? 64 : 32;
+    static constexpr int O_STAGE = 32 * OBW * 2;
+    static constexpr int OFF_OST = OFF_V + KS * KV_TILE;                // [softmax warps] (1024-aligned)
+    static constexpr int OFF_XMAX = OFF_OST + 4 * CS * NQ * O_STAGE;   // f32 [NQ][2][CS][128] (CS > 1)
+    static constexpr int OFF_XL = OFF_XMAX + (CS > 1 ? NQ * 2 * CS * 128 * 4 : 0);  // f32x2 [NQ][CS][128] (CS > 1)
+    static constexpr int OFF_FLAG = OFF_XL + (CS > 1 ? NQ * CS * 128 * 8 : 0);       // u32 [NQ] (+ pad)
     static constexpr int OFF_BAR = OFF_FLAG + 16;
     static constexpr int BAR_Q_FULL = 0;                     // [NQ]
     static constexpr int BAR_Q_EMPTY = BAR_Q_FULL + NQ;      // [NQ]
@@ -155,7 +187,8 @@ struct FwdCfg {
     static constexpr int BAR_QT_FULL = BAR_DRAIN + 1;        // [2] Q copied into TMEM buffer
     static constexpr int BAR_QT_EMPTY = BAR_QT_FULL + 2;     // [2] last S MMA read the buffer
     static constexpr int BAR_PA_READY = BAR_QT_EMPTY + 2;    // [NQ][NS][NP-1] earlier key parts of P written
-    static constexpr int NUM_BARS = BAR_PA_READY + NQ * NS * (NP > 1 ? NP - 1 : 1);
+    static constexpr int BAR_NEVER = BAR_PA_READY + NQ * NS * (NP > 1 ? NP - 1 : 1);   // nothing arrives (tests)
+    static constexpr int NUM_BARS = BAR_NEVER + 1;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_TMEM_SLOT + 16 + 1024;  // + slack for base alignment
 
@@ -189,8 +222,10 @@ struct FwdCfg {
     static_assert(!REG_SPLIT || 2 * 128 * REG_SOFTMAX + 128 * REG_CTRL <= NUM_THREADS * 168,
                   "register split exceeds the launch allocation");
 
-    static constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false, false);
-    static constexpr uint32_t IDESC_PV = ptx::idesc_bf16_f32(BM, D, false, true);
+    static constexpr uint32_t IDESC_S =
+        F8 ? ptx::idesc_e4m3_f32(BM, BN, false, false) : ptx::idesc_bf16_f32(BM, BN, false, false);
+    static constexpr uint32_t IDESC_PV =
+        F8 ? ptx::idesc_e4m3_f32(BM, D, false, true) : ptx::idesc_bf16_f32(BM, D, false, true);
 
     static_assert(D % 64 == 0 && D >= 64 && D <= 256, "D must be 64, 128 or 256");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64, 256]");
@@ -202,6 +237,13 @@ struct FwdCfg {
     static_assert(!QT || NQ == 1, "Q in TMEM needs one Q tile per unit");
     static_assert(!QT || (D / CS) % 64 == 0, "Q copy works on whole 64-column swizzle blocks");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
+    static_assert(OFF_OST % 1024 == 0 && O_STAGE % 1024 == 0,
+                  "a swizzled TMA box needs an aligned shared-memory side (1024 bytes covers both swizzles)");
+    static_assert((D / CS) % OBW == 0, "a warp's O columns are whole store boxes");
+    static_assert(!P2 || CS == 1, "two-term P keeps a row's residuals beside its own weights (one warp per row)");
+    static_assert(!F8 || (!QT && !P2 && CS == 1 && D % 128 == 0), "e4m3 path: Q in shared memory, one-term P, "
+                                                                   "one warp per row, whole 128-byte rows");
+    static_assert(NCOL % (4 * NP) == 0, "P parts are whole 32-bit TMEM columns");
 };
 
 // Number of K/V tiles a 128-row Q tile starting at q0 visits (0 if the tile is empty).
@@ -318,8 +360,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *er
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p,
-                   const __grid_constant__ SplitRanges ranges)
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const FwdParams p, const __grid_constant__ SplitRanges ranges)
 {
     using namespace ptx;
     extern __shared__ uint8_t smem_raw[];
@@ -354,6 +396,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 mbar_init(bar(C::BAR_PA_READY + i * (C::NP - 1) + q), C::GROUP_WARPS);
         }
         mbar_init(bar(C::BAR_DRAIN), 1);
+        mbar_init(bar(C::BAR_NEVER), 1);
         for (int q = 0; q < 2; ++q) {
             mbar_init(bar(C::BAR_QT_FULL + q), C::GROUP_WARPS);
             mbar_init(bar(C::BAR_QT_EMPTY + q), 1);
@@ -409,7 +452,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         mbar_arrive_expect_tx(bar(C::BAR_Q_FULL + t), C::Q_TILE);
 #pragma unroll
                         for (int c = 0; c < C::DB; ++c)
-                            tma_load_4d_hint(sbase + C::OFF_Q + t * C::Q_TILE + c * C::Q_BLOCK, &tm_q, 64 * c,
+                            tma_load_4d_hint(sbase + C::OFF_Q + t * C::Q_TILE + c * C::Q_BLOCK, &tm_q, C::ECOLS * c,
                                              q0 + t * C::BM, bh % p.H, bh / p.H, bar(C::BAR_Q_FULL + t), pol_q);
                         ++q_loads[t];
                     }
@@ -424,7 +467,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     mbar_arrive_expect_tx(bar(C::BAR_K_FULL + s), C::KV_TILE);
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
-                        tma_load_4d_hint(sbase + C::OFF_K + s * C::KV_TILE + c * C::KV_BLOCK, &tm_k, 64 * c,
+                        tma_load_4d_hint(sbase + C::OFF_K + s * C::KV_TILE + c * C::KV_BLOCK, &tm_k, C::ECOLS * c,
                                          (sg.kv_lo + j) * C::BN, bh % p.H, bh / p.H, bar(C::BAR_K_FULL + s), pol_kv);
                     k_pending = true;
                     if (!mbar_wait(bar(C::BAR_V_EMPTY + s), ph ^ 1u, p.err, ERR_PRODUCER | 2, p.wait_limit_ns)) {
@@ -434,7 +477,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     mbar_arrive_expect_tx(bar(C::BAR_V_FULL + s), C::KV_TILE);
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c)
-                        tma_load_4d_hint(sbase + C::OFF_V + s * C::KV_TILE + c * C::KV_BLOCK, &tm_v, 64 * c,
+                        tma_load_4d_hint(sbase + C::OFF_V + s * C::KV_TILE + c * C::KV_BLOCK, &tm_v, C::ECOLS * c,
                                          (sg.kv_lo + j) * C::BN, bh % p.H, bh / p.H, bar(C::BAR_V_FULL + s), pol_kv);
                     k_pending = false;
                 }
@@ -445,14 +488,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
             for (int t = 0; t < C::NQ; ++t)
                 if (q_loads[t] > 0)
-                    mbar_wait(bar(C::BAR_Q_FULL + t), (q_loads[t] - 1) & 1, p.err, ERR_DRAIN | 1, p.wait_limit_ns);
+                    mbar_wait(bar(C::BAR_Q_FULL + t), (q_loads[t] - 1) & 1, p.err, ERR_DRAIN | 1, p.drain_limit_ns);
             const uint32_t k_done = kv_iter + (k_pending ? 1u : 0u);
             for (uint32_t it = (k_done > C::KS ? k_done - C::KS : 0); it < k_done; ++it)
                 mbar_wait(bar(C::BAR_K_FULL + it % C::KS), (it / C::KS) & 1, p.err, ERR_DRAIN | 2,
-                          p.wait_limit_ns);
+                          p.drain_limit_ns);
             for (uint32_t it = (kv_iter > C::KS ? kv_iter - C::KS : 0); it < kv_iter; ++it)
                 mbar_wait(bar(C::BAR_V_FULL + it % C::KS), (it / C::KS) & 1, p.err, ERR_DRAIN | 3,
-                          p.wait_limit_ns);
+                          p.drain_limit_ns);
         }
         __syncwarp();
       } else if (warp == C::WARP_MMA) {
@@ -522,8 +565,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         } else {
                             const uint64_t dq = desc_q + static_cast<uint64_t>((t * C::Q_TILE) >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < C::D / 16; ++kk)
-                                mma_ss(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
+                            for (int kk = 0; kk < C::S_KSTEPS; ++kk)
+                                mma_ss<C::F8>(d, dq + static_cast<uint64_t>(((kk >> 2) * C::Q_BLOCK + (kk & 3) * 32) >> 4),
                                        dk + static_cast<uint64_t>(((kk >> 2) * C::KV_BLOCK + (kk & 3) * 32) >> 4),
                                        C::IDESC_S, kk > 0 ? 1u : 0u);
                         }
@@ -560,7 +603,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         const uint32_t d = tmem + C::TM_O + t * C::D;
                         const uint32_t a = tmem + C::TM_S + (t * C::NS + b) * C::BN;
                         const uint64_t dv = desc_v + static_cast<uint64_t>((s * C::KV_TILE) >> 4);
-                        constexpr int KP = C::BN / 16 / C::NP;   // K steps per part of P
+                        constexpr int KP = C::PV_KSTEPS / C::NP;   // K steps per part of P
 #pragma unroll
                         for (int q = 0; q < C::NP; ++q) {
                             if (q > 0) {
@@ -570,8 +613,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                             }
 #pragma unroll
                             for (int kk = q * KP; kk < (q + 1) * KP; ++kk)
-                                mma_ts(d, a + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4), C::IDESC_PV,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
+                                mma_ts<C::F8>(d, a + kk * 8, dv + static_cast<uint64_t>((kk * C::PV_KSTEP_BYTES) >> 4),
+                                              C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                            if constexpr (C::P2) {   // the residual weights, from the buffer's upper half
+#pragma unroll
+                                for (int kk = q * KP; kk < (q + 1) * KP; ++kk)
+                                    mma_ts(d, a + C::BN / 2 + kk * 8,
+                                           dv + static_cast<uint64_t>((kk * C::PV_KSTEP_BYTES) >> 4), C::IDESC_PV, 1u);
+                            }
                         }
                         mma_commit(bar(C::BAR_O_DONE + t));
                         if (last_user(j) == t)
@@ -624,7 +673,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             // drain: every MMA issued above has completed before TMEM can be released
             mma_commit(bar(C::BAR_DRAIN));
-            lone_wait(bar(C::BAR_DRAIN), 0, p.err, ERR_DRAIN | 4, p.wait_limit_ns);
+            lone_wait(bar(C::BAR_DRAIN), 0, p.err, ERR_DRAIN | 4, p.drain_limit_ns);
         }
         __syncwarp();
       }
@@ -638,9 +687,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t o_addr = tmem + lane_base + C::TM_O + t * C::D + h * C::OCOL;
+        const uint32_t o_stage = sbase + C::OFF_OST + warp * C::O_STAGE;   // this warp's O staging
         const uint32_t xmax = sbase + C::OFF_XMAX + t * (2 * C::CS * 128 * 4);
         const uint32_t xl = sbase + C::OFF_XL + t * (C::CS * 128 * 8);
-        const float c2 = p.scale_log2;
         // one arrival per warp: every lane's prior writes (shared memory, and TMEM
         // after its own wait + fence) are ordered before lane 0's arrive by the
         // __syncwarp, and the arrive releases them to the waiting side
@@ -651,7 +700,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         };
         uint32_t tbase = 0;    // S tiles of this slot in earlier segments (running phase base)
         uint32_t group_uses = 0;   // completed phases of this slot's group barrier
-        bool ok = true;
+        // tests of the time-out path: a wait that must run out (the other roles' waits on
+        // these warps then run out too, and every CTA drains its own work and exits)
+        bool ok = !p.stall_test ||
+                  warp_wait(bar(C::BAR_NEVER), 0, p.err, ERR_SOFTMAX | 0xF, p.wait_limit_ns);
         // QT: copy the next Q tile from shared memory into TMEM buffer (q_copies % QB).
         // Each thread moves its own row's slice of D/CS columns: 16-byte pieces of the
         // 128B-swizzled rows (piece c of row r sits at c ^ (r % 8)) become packed bf16
@@ -691,6 +743,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             decode_unit(sg.unit, p, qg, bh);
             const int q0_t = qg * (C::NQ * C::BM) + t * C::BM;
             const int grow = q0_t + row;             // query index
+            // score multiplier in log2 units (e4m3: the head's Q and K descales folded in)
+            const float c2 = C::F8 ? p.scale_log2 * __ldg(p.descale_q + bh) * __ldg(p.descale_k + bh) : p.scale_log2;
             const int n = segment_tiles(sg, q0_t, p, C::BN);
             if (n == 0)
                 continue;
@@ -839,8 +893,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const uint64_t negm2 = f32x2(-m_sub, -m_sub);
                 uint64_t ls01 = 0, ls23 = 0;   // packed (0.f, 0.f)
                 float lr0 = 0.f, lr1 = 0.f;
-                uint32_t pk[C::NCOL / 2];
-                const uint32_t p_addr = s_addr + h * (C::NCOL / 2);
+                uint32_t pk[C::PW];
+                uint32_t pl[C::P2 ? C::PW : 1];   // P2: the residual terms
+                const uint32_t p_addr = s_addr + h * C::PW;
                 // weights of columns [CB, CE) into pk (bf16 pairs) and the two sums
                 auto exp_cols = [&](auto cb, auto ce) {
                     constexpr int CB = decltype(cb)::value, CE = decltype(ce)::value;
@@ -849,40 +904,72 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         float x0, x1, x2, x3;
                         unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), c2x2, negm2), x0, x1);
                         unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), c2x2, negm2), x2, x3);
-                        const float p0 = ex2_approx(x0);
-                        const float p1 = ex2_approx(x1);
-                        const float p2 = ex2_approx(x2);
-                        const float p3 = ex2_approx(x3);
-                        const uint32_t w0 = pack_bf16x2(p0, p1);
-                        const uint32_t w1 = pack_bf16x2(p2, p3);
-                        pk[c / 2] = w0;
-                        pk[c / 2 + 1] = w1;
+                        float p0, p1, p2, p3;
+                        // the first FA2_EXP2_EMU_PAIRS column pairs of every 32 go to the FMA pipe
+                        // (c is a constant in each unrolled iteration, so the choice is static)
+                        const int pair = (c % 32) / 2;
+                        if (pair < FA2_EXP2_EMU_PAIRS) {
+                            unpack_f32x2(exp2_poly_f32x2(x0, x1), p0, p1);
+                        } else {
+                            p0 = ex2_approx(x0);
+                            p1 = ex2_approx(x1);
+                        }
+                        if (pair + 1 < FA2_EXP2_EMU_PAIRS) {
+                            unpack_f32x2(exp2_poly_f32x2(x2, x3), p2, p3);
+                        } else {
+                            p2 = ex2_approx(x2);
+                            p3 = ex2_approx(x3);
+                        }
                         ls01 = add_f32x2(ls01, f32x2(p0, p1));
                         ls23 = add_f32x2(ls23, f32x2(p2, p3));
-                        lr0 = add_bf16x2_to_f32(lr0, w0);
-                        lr1 = add_bf16x2_to_f32(lr1, w1);
+                        if constexpr (C::F8) {
+                            // four keys per TMEM column; l_o sums the e4m3 values the MMA sees
+                            const uint32_t w = pack_e4m3x4(p0, p1, p2, p3);
+                            pk[c / 4] = w;
+                            lr0 = add_e4m3x4_to_f32(lr0, w);
+                        } else {
+                            const uint32_t w0 = pack_bf16x2(p0, p1);
+                            const uint32_t w1 = pack_bf16x2(p2, p3);
+                            pk[c / 2] = w0;
+                            pk[c / 2 + 1] = w1;
+                            if constexpr (C::P2) {
+                                // p - bf16(p) is exact in fp32; rounding it to bf16 leaves p_hi + p_lo
+                                // within about 2^-17 of p, so O is divided by the exact sum l
+                                pl[c / 2] = pack_bf16x2_of_f32x2(sub_f32x2(f32x2(p0, p1), widen_bf16x2(w0)));
+                                pl[c / 2 + 1] = pack_bf16x2_of_f32x2(sub_f32x2(f32x2(p2, p3), widen_bf16x2(w1)));
+                            } else {
+                                lr0 = add_bf16x2_to_f32(lr0, w0);
+                                lr1 = add_bf16x2_to_f32(lr1, w1);
+                            }
+                        }
                     }
                 };
                 // words [W0, W0 + NW) of pk to their TMEM columns
                 auto store_words = [&](auto w0, auto nw) {
                     constexpr int W0 = decltype(w0)::value, NW = decltype(nw)::value;
                     static_assert(NW % 32 == 0 || NW == 16 || NW == 8, "P stores move 8, 16 or 32 columns at a time");
-                    if constexpr (NW % 32 == 0) {
+                    auto put = [&](uint32_t addr, const uint32_t *src) {
+                        if constexpr (NW % 32 == 0) {
 #pragma unroll
-                        for (int q = 0; q < NW / 32; ++q)
-                            tmem_st32(p_addr + W0 + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(pk + W0 + 32 * q));
-                    } else if constexpr (NW == 16) {
-                        tmem_st16(p_addr + W0, pk + W0);
-                    } else {
-                        tmem_st8(p_addr + W0, pk + W0);
-                    }
+                            for (int q = 0; q < NW / 32; ++q)
+                                tmem_st32(addr + 32 * q, *reinterpret_cast<const uint32_t(*)[32]>(src + 32 * q));
+                        } else if constexpr (NW == 16) {
+                            tmem_st16(addr, src);
+                        } else {
+                            tmem_st8(addr, src);
+                        }
+                    };
+                    put(p_addr + W0, pk + W0);
+                    if constexpr (C::P2)   // residual terms over the buffer's upper half
+                        put(p_addr + C::BN / 2 + W0, pl + W0);
                 };
                 // part q of NP: its weights, stored, and (all but the last) handed to the
                 // MMA warp before the next part is computed
                 auto part = [&](auto qc) {
                     constexpr int Q = decltype(qc)::value, PC = C::NCOL / C::NP;
                     exp_cols(std::integral_constant<int, Q * PC>{}, std::integral_constant<int, (Q + 1) * PC>{});
-                    store_words(std::integral_constant<int, Q * PC / 2>{}, std::integral_constant<int, PC / 2>{});
+                    store_words(std::integral_constant<int, Q * PC * C::EB / 4>{},
+                                std::integral_constant<int, PC * C::EB / 4>{});
                     if constexpr (Q < C::NP - 1) {
                         tmem_st_wait();
                         tc_fence_before();
@@ -902,7 +989,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     unpack_f32x2(ls23, a2, a3);
                     l = l * alpha + ((a0 + a1) + (a2 + a3));
                 }
-                l_o = l_o * alpha + (lr0 + lr1);
+                if constexpr (C::P2)
+                    l_o = l;   // the two terms together carry p itself
+                else
+                    l_o = l_o * alpha + (lr0 + lr1);
                 if (j > 0 && !grow_any && j == n - 1) {
                     ok = warp_wait(bar(C::BAR_O_DONE + t), (g - 1) & 1, p.err, ERR_SOFTMAX | 2, p.wait_limit_ns);
                     if (!ok)
@@ -955,13 +1045,39 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 }
             }
             tc_fence_after();
-            const float inv_l = 1.f / lo_tot;
+            // 1/l_o, times the head's V descale for e4m3 inputs
+            const float inv_l = (C::F8 ? __ldg(p.descale_v + bh) : 1.f) / lo_tot;
             const bool live = grow < p.Lq;
             const size_t out_row = static_cast<size_t>(bh) * p.Lq + (live ? grow : 0);
-            uint16_t *orow = p.o + static_cast<long long>(bh / p.H) * p.o_sb +
-                             static_cast<long long>(bh % p.H) * p.o_sh +
-                             static_cast<long long>(live ? grow : 0) * p.o_sl + h * C::OCOL;
             const bool whole = sg.c_first == sg.c_last;
+            // O leaves through the warp's staging buffer, one OBW-column block at a time:
+            // o_block_begin waits until the previous TMA store has read the buffer,
+            // o_block_put writes 16 bf16 words (32 columns) of this thread's row, and
+            // o_block_store writes the warp's 32 rows x OBW columns with one TMA store
+            // (whole lines of its rows; rows past Lq lie outside the tensor map and are
+            // not written).
+            auto o_block_begin = [&]() {
+                if (lane == 0)
+                    bulk_wait_group_read0();
+                __syncwarp();
+            };
+            // (16-byte chunk k of row r sits at k ^ (r % 8) in 128-byte rows under the 128B
+            // swizzle, at k ^ ((r / 2) % 4) in 64-byte rows under the 64B swizzle)
+            auto o_block_put = [&](int hf, const uint32_t (&w)[16]) {
+                const uint32_t rowp = o_stage + lane * (C::OBW * 2);
+                const int sw = C::OBW == 64 ? (lane & 7) : ((lane >> 1) & 3);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    st_shared_v4(rowp + (((4 * hf + c) ^ sw) * 16), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            };
+            auto o_block_store = [&](int bq) {
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0 && q0_t + quarter * 32 < p.Lq) {
+                    tma_store_4d(&tm_o, o_stage, h * C::OCOL + C::OBW * bq, q0_t + quarter * 32, bh % p.H, bh / p.H);
+                    bulk_commit_group();
+                }
+            };
             // this part's workspace rows (cut units only): LSE pairs by row, O as float4
             // column groups of 128 rows each
             const size_t part_tile = (static_cast<size_t>(blockIdx.x) * 2 + sg.slot) * C::NQ + t;
@@ -1005,7 +1121,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const float inv_w = 1.f / wsum;
                 const float4 *part4 = reinterpret_cast<const float4 *>(p.part_o);
 #pragma unroll 1
-                for (int cc = 0; cc < C::OCOL / 32; ++cc) {
+                for (int bq = 0; bq < C::OCOL / C::OBW; ++bq) {
+                  o_block_begin();
+#pragma unroll
+                  for (int hf = 0; hf < C::OBW / 32; ++hf) {
+                    const int cc = (C::OBW / 32) * bq + hf;
                     const size_t col4 = static_cast<size_t>((h * C::OCOL + 32 * cc) / 4) * 128 + row;
                     // this CTA's own part, read out of TMEM when its turn in the sum comes
                     auto load_own = [&](float4 *dst) {
@@ -1058,15 +1178,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                             acc[4 * q + 3] += wa * va[q].w + wb * vb[q].w;
                         }
                     }
-                    if (live) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
+                    uint32_t w[16];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(pack_bf16x2(acc[8 * q], acc[8 * q + 1]),
-                                                pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]),
-                                                pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]),
-                                                pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]));
-                    }
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+                    o_block_put(hf, w);
+                  }
+                  o_block_store(bq);
                 }
                 if (h == 0 && live)
                     p.lse[out_row] = (mx + lg2_approx(xsum)) * LN2;
@@ -1095,35 +1213,37 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             } else {
                 float4 *ptile = whole ? nullptr : reinterpret_cast<float4 *>(p.part_o) + part_tile * (C::D / 4) * 128;
 #pragma unroll 1
-                for (int cc = 0; cc < C::OCOL / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + 32 * cc, r);
-                    tmem_ld_wait(r);
-                    if (cc == C::OCOL / 32 - 1) {
-                        // every read of O_t is done: the next segment's first PV may overwrite it
-                        tc_fence_before();
-                        warp_arrive(bar(C::BAR_O_FREE + t));
-                    }
-                    if (whole) {
-                        uint32_t w[16];
+                for (int bq = 0; bq < C::OCOL / C::OBW; ++bq) {
+                    if (whole)
+                        o_block_begin();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
-                                               __uint_as_float(r[2 * e + 1]) * inv_l);
-                        if (live) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * cc);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    for (int hf = 0; hf < C::OBW / 32; ++hf) {
+                        const int cc = (C::OBW / 32) * bq + hf;
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + 32 * cc, r);
+                        tmem_ld_wait(r);
+                        if (cc == C::OCOL / 32 - 1) {
+                            // every read of O_t is done: the next segment's first PV may overwrite it
+                            tc_fence_before();
+                            warp_arrive(bar(C::BAR_O_FREE + t));
                         }
-                    } else {
-                        const int g0 = (h * C::OCOL + 32 * cc) / 4;   // first float4 column group
+                        if (whole) {
+                            uint32_t w[16];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            ptile[(g0 + q) * 128 + row] = make_float4(
-                                __uint_as_float(r[4 * q]) * inv_l, __uint_as_float(r[4 * q + 1]) * inv_l,
-                                __uint_as_float(r[4 * q + 2]) * inv_l, __uint_as_float(r[4 * q + 3]) * inv_l);
+                            for (int e = 0; e < 16; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+                            o_block_put(hf, w);
+                        } else {
+                            const int g0 = (h * C::OCOL + 32 * cc) / 4;   // first float4 column group
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                ptile[(g0 + q) * 128 + row] = make_float4(
+                                    __uint_as_float(r[4 * q]) * inv_l, __uint_as_float(r[4 * q + 1]) * inv_l,
+                                    __uint_as_float(r[4 * q + 2]) * inv_l, __uint_as_float(r[4 * q + 3]) * inv_l);
+                        }
                     }
+                    if (whole)
+                        o_block_store(bq);
                 }
                 if (whole) {
                     if (h == 0 && live)
@@ -1156,6 +1276,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             tbase += n;
         }
+        // a loop left early (a wait that ran out) may leave P stores in flight
+        tmem_st_wait();
+        if (lane == 0)   // O stores complete before the CTA (and its staging buffer) goes
+            bulk_wait_group0();
+        __syncwarp();
     }
 
     // ---- teardown

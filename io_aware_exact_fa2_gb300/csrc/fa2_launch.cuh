@@ -32,13 +32,17 @@ struct LaunchArgs {
     const void *q, *k, *v;
     void *o;
     float *lse;
+    // e4m3 inputs only (fa2_fwd_fp8): fp32 [B*H] descales, real input = stored value x descale
+    const float *descale_q = nullptr, *descale_k = nullptr, *descale_v = nullptr;
     int B, H, Lq, Lk;
     BhlStrides sq, sk, sv, so;   // element strides of Q, K, V, O
     int causal;
     int window;               // causal sliding window, -1: none
     float scale_log2;
     int *err;
-    unsigned long long wait_limit_ns;
+    unsigned long long wait_limit_ns;    // waits between warps
+    unsigned long long drain_limit_ns;   // a CTA's waits for its own copies and MMAs before exit
+    int stall_test = 0;       // tests only: make the softmax warps' first wait run out
     cudaStream_t stream;
     EncodeTiledFn encode;
     int device;
@@ -131,19 +135,24 @@ size_t workspace_bytes_for(int B, int H, int Lq, int Lk, int causal, int num_sms
 }
 
 // 4-D view of a bf16 [B, H, L, D] tensor with contiguous rows of D and the given
-// element strides: dims (D, L, H, B) innermost first, a box of 64 columns (128 bytes,
-// one swizzle span) by box_rows rows of one head.  Rows outside [0, L) read as zero.
+// element strides: dims (D, L, H, B) innermost first, a box of box_cols columns (64:
+// 128 bytes under the 128B swizzle; 32: 64 bytes under the 64B swizzle -- one swizzle
+// span either way) by box_rows rows of one head.  Loads read rows outside [0, L) as
+// zero; stores leave them unwritten.
 inline bool encode_bhld_strided(EncodeTiledFn encode, CUtensorMap *m, const void *ptr, int D, int L, int H, int B,
-                                BhlStrides st, int box_rows)
+                                BhlStrides st, int box_rows, int box_cols = 64, int elem_bytes = 2)
 {
+    // elem_bytes 1: e4m3 bytes (moved as raw bytes), the box then 128 elements wide
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(B)};
-    cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.l) * 2, static_cast<cuuint64_t>(st.h) * 2,
-                             static_cast<cuuint64_t>(st.b) * 2};
-    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.l) * elem_bytes, static_cast<cuuint64_t>(st.h) * elem_bytes,
+                             static_cast<cuuint64_t>(st.b) * elem_bytes};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUtensorMapSwizzle sw = box_cols * elem_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = encode(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -152,21 +161,24 @@ template <class C>
 fa2_status launch_fwd(const LaunchArgs &a)
 {
     const int BH = a.B * a.H;
-    CUtensorMap tq, tk, tv;
-    if (!encode_bhld_strided(a.encode, &tq, a.q, C::D, a.Lq, a.H, a.B, a.sq, C::BM) ||
-        !encode_bhld_strided(a.encode, &tk, a.k, C::D, a.Lk, a.H, a.B, a.sk, C::BN) ||
-        !encode_bhld_strided(a.encode, &tv, a.v, C::D, a.Lk, a.H, a.B, a.sv, C::BN))
+    CUtensorMap tq, tk, tv, to;
+    // O is written by TMA stores of 32 rows x OBW columns (one softmax warp's rows)
+    if (!encode_bhld_strided(a.encode, &tq, a.q, C::D, a.Lq, a.H, a.B, a.sq, C::BM, C::ECOLS, C::EB) ||
+        !encode_bhld_strided(a.encode, &tk, a.k, C::D, a.Lk, a.H, a.B, a.sk, C::BN, C::ECOLS, C::EB) ||
+        !encode_bhld_strided(a.encode, &tv, a.v, C::D, a.Lk, a.H, a.B, a.sv, C::BN, C::ECOLS, C::EB) ||
+        !encode_bhld_strided(a.encode, &to, a.o, C::D, a.Lq, a.H, a.B, a.so, 32, C::OBW))
         return FA2_ERR_CUDA;
 
     FwdParams p;
-    p.o = static_cast<uint16_t *>(a.o);
-    p.o_sb = a.so.b;
-    p.o_sh = a.so.h;
-    p.o_sl = a.so.l;
     p.H = a.H;
+    p.descale_q = a.descale_q;
+    p.descale_k = a.descale_k;
+    p.descale_v = a.descale_v;
     p.lse = a.lse;
     p.err = a.err;
     p.wait_limit_ns = a.wait_limit_ns;
+    p.drain_limit_ns = a.drain_limit_ns;
+    p.stall_test = a.stall_test;
     p.Lq = a.Lq;
     p.Lk = a.Lk;
     p.BH = BH;
@@ -214,7 +226,7 @@ fa2_status launch_fwd(const LaunchArgs &a)
         }
         configured.fetch_or(bit);
     }
-    fa2_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p, ranges);
+    fa2_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, to, p, ranges);
     return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
@@ -250,6 +262,7 @@ constexpr size_t bwd_stats_bytes(int B, int H, int Lq)
 fa2_status launch_fwd_d64(const LaunchArgs &a);
 fa2_status launch_fwd_d128(const LaunchArgs &a);
 fa2_status launch_fwd_d256(const LaunchArgs &a);
+fa2_status launch_fwd_fp8_d128(const LaunchArgs &a);   // e4m3 Q, K, V (fa2_fwd_fp8_d128.cu)
 size_t workspace_bytes_d64(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy);
 size_t workspace_bytes_d128(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy);
 size_t workspace_bytes_d256(int B, int H, int Lq, int Lk, int causal, int num_sms, int policy);

@@ -189,6 +189,36 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// 4-D tiled store shared -> global of one box, tracked by this thread's bulk async-group.
+// Elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const void *tmap, uint32_t src, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until this thread's bulk stores have finished reading their shared-memory source.
+__device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Make this thread's shared-memory writes visible to the async proxy (a TMA store
+// that reads them).
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_last()
 {
     uint64_t p;
@@ -236,28 +266,47 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem] * B[smem]^T-by-descriptor, kind::f16 (bf16 in, fp32 accumulate).
+// D[tmem] (+)= A[smem] * B[smem]^T-by-descriptor, fp32 accumulate: kind::f16 (bf16
+// operands) or, with F8, kind::f8f6f4 (e4m3 operands).
+template <bool F8 = false>
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (F8)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16.
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16 or (F8) kind::f8f6f4.
+template <bool F8 = false>
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (F8)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
@@ -389,6 +438,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B and an fp32 accumulator:
+// the layout of idesc_bf16_f32 with the A and B format fields holding e4m3 (0).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ------------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x)
 {
@@ -441,6 +498,92 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Packed bf16 pair -> fp32 pair (exact: a bf16 is the high half of an fp32); the
+// low half of w becomes the low float.
+__device__ __forceinline__ uint64_t widen_bf16x2(uint32_t w)
+{
+    return static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xffff0000u) << 32);
+}
+
+// 2^x for a pair of fp32 x <= 128 on the FMA and integer pipes instead of the MUFU
+// (Cody-Waite range reduction x = n + f, n = floor(x), f in [0, 1), then 2^f from a
+// degree-3 polynomial and 2^n added into the exponent field).  The coefficients are
+// the relative-error minimax fit of 2^f on [0, 1] from the Remez exchange algorithm:
+// |p(f) / 2^f - 1| <= 7.5e-5 (bf16 weights round at 2^-9).  x is clamped below at
+// -126 (the smallest exponent the field add cannot wrap), so masked entries (-inf)
+// give about 2^-126 instead of 0.
+__device__ __forceinline__ uint64_t exp2_poly_f32x2(float x0, float x1)
+{
+    constexpr float SHIFT = 12582912.0f;   // 1.5 * 2^23: adding it (rounding down) leaves floor(x) in the low bits
+    const uint64_t x = f32x2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+    uint64_t y, n, f, p;
+    const uint64_t sh = f32x2(SHIFT, SHIFT);
+    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(sh));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(n) : "l"(y), "l"(sh));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(f) : "l"(x), "l"(n));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(f), "l"(f32x2(0.07802452f, 0.07802452f)),
+        "l"(f32x2(0.22606716f, 0.22606716f)));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(p), "l"(f), "l"(f32x2(0.69583356f, 0.69583356f)));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(p), "l"(f), "l"(f32x2(0.99992520f, 0.99992520f)));
+    // floor(x) sits in the low bits of y's pattern (two's complement over the low 9
+    // bits); shifted into the exponent field it scales p(f) by 2^n
+    const uint32_t ylo = static_cast<uint32_t>(y), yhi = static_cast<uint32_t>(y >> 32);
+    const uint32_t plo = static_cast<uint32_t>(p) + (ylo << 23);
+    const uint32_t phi = static_cast<uint32_t>(p >> 32) + (yhi << 23);
+    return static_cast<uint64_t>(plo) | (static_cast<uint64_t>(phi) << 32);
+}
+
+// Four fp32 -> four e4m3 in one word (round to nearest even, saturating at +-448),
+// a0 in bits [0,8) ... a3 in bits [24,32).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    return r;
+}
+
+// acc + the four e4m3 values of w, each widened exactly (e4m3 -> f16) and added in fp32.
+__device__ __forceinline__ float add_e4m3x4_to_f32(float acc, uint32_t w)
+{
+    asm("{\n\t.reg .b16 lo, hi, f0, f1, f2, f3;\n\t.reg .b32 h01, h23;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h01, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h23, hi;\n\t"
+        "mov.b32 {f0, f1}, h01;\n\t"
+        "mov.b32 {f2, f3}, h23;\n\t"
+        "add.rn.f32.f16 %0, f0, %0;\n\t"
+        "add.rn.f32.f16 %0, f1, %0;\n\t"
+        "add.rn.f32.f16 %0, f2, %0;\n\t"
+        "add.rn.f32.f16 %0, f3, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w));
+    return acc;
+}
+
+// fp32 pair -> packed bf16 pair (round to nearest even), the low float in bits [0,16).
+__device__ __forceinline__ uint32_t pack_bf16x2_of_f32x2(uint64_t v)
+{
+    uint32_t r;
+    asm("{\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 {lo, hi}, %1;\n\t"
+        "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "l"(v));
+    return r;
 }
 
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)

@@ -78,5 +78,30 @@ def make_qkv(B: int, H: int, Lq: int, Lk: int, D: int, seed_base: int,
     return q, k, v
 
 
+def make_qkv_fp8(B: int, H: int, Lq: int, Lk: int, D: int, seed_base: int):
+    """Seeded e4m3 (torch.float8_e4m3fn) q, k, v with fp32 descales of shape (B, H).
+
+    The fp32 N(0, 1) draws are those of ``make_qkv`` (same seeds, before any bf16
+    rounding).  Each (b, h) slice is divided by its descale = max|x| / 448 (e4m3's
+    largest finite value; 1 for an all-zero slice) and cast to e4m3 (round to
+    nearest even); the real input the pair stands for is stored value x descale.
+    Returns (q8, k8, v8, dq, dk, dv), descales as float32 numpy arrays.
+    """
+    import numpy as np
+
+    def quant(shape, seed):
+        g = torch.Generator(device="cpu")
+        g.manual_seed(int(seed))
+        x = torch.randn(tuple(shape), generator=g, dtype=torch.float32)
+        amax = x.abs().amax(dim=(2, 3))
+        ds = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        return (x / ds[:, :, None, None]).to(torch.float8_e4m3fn), ds.numpy().astype(np.float32)
+
+    q8, dq = quant((B, H, Lq, D), seed_base + 0)
+    k8, dk = quant((B, H, Lk, D), seed_base + 1)
+    v8, dv = quant((B, H, Lk, D), seed_base + 2)
+    return q8, k8, v8, dq, dk, dv
+
+
 def workload_inputs(w: Workload):
     return make_qkv(w.B, w.H, w.Lq, w.Lk, w.D, w.seed_base, w.peaky_every, w.peaky_factor)

@@ -17,12 +17,17 @@ Flash Attention -- blocked attention" (sections 3 and 4).
 
 It also holds the backward definition of the same attention (Chapter 08,
 section 6: Delta, the softmax backward, dV = P^T dO, dK = scale dS^T Q,
-dQ = scale dS K) and an fp64-input forward for numerical differentiation.
+dQ = scale dS K), an fp64-input forward for numerical differentiation, and the
+FP8 forward's reference: e4m3 inputs with per-(batch, head) descales, widened
+exactly and fed to the same definition.
 
 Every function here is pinned: the forward by ``tests/test_oracle_pins.py``
 (closed forms, invariants, brute force, a library cross-check), the gradients
 by ``tests/test_oracle_grad_pins.py`` (finite differences of the forward,
-torch autograd, invariants, a closed form); none is "parity unpinned".
+torch autograd, invariants, a closed form), the FP8 inputs by
+``tests/test_oracle_fp8_pins.py`` (the e4m3 widening against torch's over all 256
+codes, agreement with the bf16 path on shared values, descale laws, closed
+forms); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -78,6 +83,17 @@ def _load():
             lib.fa2_oracle_decode_bf16.restype = None
             lib.fa2_oracle_decode_bf16.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+            lib.fa2_oracle_decode_e4m3.restype = None
+            lib.fa2_oracle_decode_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+            lib.fa2_oracle_dequant_e4m3.restype = None
+            lib.fa2_oracle_dequant_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                    ctypes.c_int64, ctypes.c_void_p]
+            lib.fa2_oracle_rows_f64.restype = ctypes.c_int
+            lib.fa2_oracle_rows_f64.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.fa2_oracle_max_threads.restype = ctypes.c_int
             lib.fa2_oracle_max_threads.argtypes = []
             i64, vp = ctypes.c_int64, ctypes.c_void_p
@@ -106,6 +122,67 @@ def decode_bf16(bits: np.ndarray) -> np.ndarray:
     out = np.empty(bits.shape, dtype=np.float64)
     _load().fa2_oracle_decode_bf16(bits.ctypes.data, out.ctypes.data, bits.size)
     return out
+
+
+def _e4m3_bits(t) -> np.ndarray:
+    """float8_e4m3fn (or uint8) torch tensor (CPU) -> contiguous uint8 numpy array of its bits."""
+    import torch
+    if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError(f"fp8 oracle inputs must be float8_e4m3fn, got {t.dtype}")
+    t = t.detach().to("cpu").contiguous()
+    return t.view(torch.uint8).numpy()
+
+
+def decode_e4m3(bits: np.ndarray) -> np.ndarray:
+    """Widen e4m3 bit patterns to fp64 the way the oracle does internally."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint8)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().fa2_oracle_decode_e4m3(bits.ctypes.data, out.ctypes.data, bits.size)
+    return out
+
+
+def dequant_e4m3(x, descale) -> np.ndarray:
+    """Real values of an e4m3 tensor (B, H, L, D) with fp32 descales (B, H): stored value x descale."""
+    bits = _e4m3_bits(x)
+    B, H, L, D = bits.shape
+    ds = np.ascontiguousarray(np.asarray(descale, dtype=np.float32).reshape(B * H))
+    out = np.empty((B, H, L, D), dtype=np.float64)
+    _load().fa2_oracle_dequant_e4m3(bits.ctypes.data, ds.ctypes.data, B * H, L * D, out.ctypes.data)
+    return out
+
+
+def rows_f64(q, k, v, causal: bool, scale: float, rows=None, threads: int = 0, window=None):
+    """Attention rows of fp64 inputs (B, H, L, D): (o (n, D), lse (n,)), as attention_rows."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    if rows is None:
+        rows = np.arange(B * H * Lq, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    o = np.empty((n, D))
+    lse = np.empty((n,))
+    rc = _load().fa2_oracle_rows_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Lq, Lk, D,
+                                      int(bool(causal)), _window_arg(causal, window, Lq, Lk), float(scale),
+                                      rows.ctypes.data if n else None, n, o.ctypes.data, lse.ctypes.data,
+                                      int(threads))
+    if rc != 0:
+        raise RuntimeError(f"fa2_oracle_rows_f64 failed with code {rc}")
+    return o, lse
+
+
+def attention_fp8(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool, scale: float, rows=None,
+                  threads: int = 0):
+    """Oracle for the FP8 forward: e4m3 q8 (B, H, Lq, D), k8, v8 (B, H, Lk, D) with fp32
+    descales (B, H) each; the real inputs are stored value x descale ("Flash Attention:
+    principles and implementation", section 4.3, names FlashAttention-3's FP8 mode; this
+    per-(batch, head) descale is the reading taken).  Exact attention of the dequantised
+    inputs in fp64.  rows: flat row ids (b*H + h)*Lq + i, None for all.
+    Returns (o (n, D), lse (n,)) fp64."""
+    q = dequant_e4m3(q8, descale_q)
+    k = dequant_e4m3(k8, descale_k)
+    v = dequant_e4m3(v8, descale_v)
+    return rows_f64(q, k, v, causal, scale, rows, threads)
 
 
 def max_threads() -> int:

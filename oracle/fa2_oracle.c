@@ -21,7 +21,7 @@
  *     pass needs; section 4 ("causal mask"): query i may see key j only when
  *     j <= i (lower triangle including the diagonal).
  *
- * Readings taken where the pages are loose (each listed in the design doc):
+ * Readings taken where the pages are loose:
  *   - LSE is the NATURAL log of sum_j exp(s_ij) over the SCALED scores
  *     s_ij = scale * q_i . k_j (the plain definition; page 4's base-2 value is
  *     this times log2(e)).
@@ -387,6 +387,89 @@ int fa2_oracle_bwd_f64(const double *q, const double *k, const double *v, const 
         free(p);
         free(dp);
         free(o_row);
+    }
+    return failed ? 2 : 0;
+}
+
+/*
+ * ------------------------------------------------------------------ FP8 inputs
+ *
+ * The FP8 forward that "Flash Attention: principles and implementation"
+ * (tbr8.org), section 4.3, names for FlashAttention-3 without fixing a format.
+ * Reading taken: Q, K and V are stored as e4m3 (1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; no infinities, exponent 15 with mantissa 7 is NaN;
+ * largest finite value 448), each with one fp32 descale factor per (batch, head):
+ * the real input is the stored value times its descale.  The oracle widens the
+ * stored values exactly, multiplies by the descale in fp64 (exact: at most 4 + 24
+ * significant bits), and applies the attention definition above unchanged.
+ */
+static double e4m3_to_f64(uint8_t bits)
+{
+    const int sign = bits >> 7, e = (bits >> 3) & 0xF, m = bits & 0x7;
+    if (e == 15 && m == 7)
+        return NAN;
+    /* subnormal (e = 0): m/8 * 2^-6;  normal: (1 + m/8) * 2^(e - 7) */
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(8.0 + (double)m, e - 10);
+    return sign ? -mag : mag;
+}
+
+/* Exposed so a test can pin the widening against an independent decoder. */
+void fa2_oracle_decode_e4m3(const uint8_t *src, double *dst, int64_t n)
+{
+    for (int64_t t = 0; t < n; ++t)
+        dst[t] = e4m3_to_f64(src[t]);
+}
+
+/*
+ * Real values of an e4m3 tensor (BH heads of `per_head` elements, contiguous):
+ * out[h][e] = e4m3(x[h][e]) * descale[h].
+ */
+void fa2_oracle_dequant_e4m3(const uint8_t *x, const float *descale, int64_t BH, int64_t per_head, double *out)
+{
+    for (int64_t h = 0; h < BH; ++h)
+        for (int64_t e = 0; e < per_head; ++e)
+            out[h * per_head + e] = e4m3_to_f64(x[h * per_head + e]) * (double)descale[h];
+}
+
+/*
+ * Attention for a list of output rows of fp64 inputs (contiguous (B, H, L, D)):
+ * the same row definition as fa2_oracle_rows_w.  Returns as fa2_oracle_rows_w.
+ */
+int fa2_oracle_rows_f64(const double *q, const double *k, const double *v, int64_t B, int64_t H, int64_t Lq,
+                        int64_t Lk, int64_t D, int causal, int64_t window, double scale, const int64_t *rows,
+                        int64_t n_rows, double *o, double *lse, int n_threads)
+{
+    if (!q || !k || !v || !o || !lse || (n_rows > 0 && !rows))
+        return 1;
+    if (B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0 || n_rows < 0)
+        return 1;
+    for (int64_t r = 0; r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= B * H * Lq)
+            return 1;
+    int failed = 0;
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)Lk * sizeof(double));
+        double *p = (double *)malloc((size_t)Lk * sizeof(double));
+        if (!s || !p) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t r = 0; r < n_rows; ++r) {
+                const int64_t bh = rows[r] / Lq, i = rows[r] % Lq;
+                one_row_f64(q + rows[r] * D, k + bh * Lk * D, v + bh * Lk * D, i, Lk, D, causal, window, scale,
+                            s, p, o + r * D, lse + r);
+            }
+        }
+        free(s);
+        free(p);
     }
     return failed ? 2 : 0;
 }

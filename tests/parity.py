@@ -57,6 +57,8 @@ def compare(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, o_ref: np.ndarray, lse_r
     rep = {"max_dO": float(d_o.max()) if d_o.size else 0.0,
            "max_dLSE": float(d_l.max()) if d_l.size else 0.0,
            "n_bigO": int((np.abs(o_ref) >= 4.0).sum()),
+           # elements above the flat 1e-2 (only the |O| >= 4 allowance may admit them)
+           "n_over_flat": int((d_o > O_TOL).sum()),
            "n": int(o_ref.size)}
     if bad_o.any():
         idx = np.argwhere(bad_o)[:5]

@@ -33,7 +33,7 @@ def header_functions():
 
 def test_header_declares_the_boundary():
     assert header_functions() == ["fa2_bwd", "fa2_bwd_ex", "fa2_bwd_window", "fa2_bwd_workspace_size", "fa2_fwd",
-                                  "fa2_fwd_ex",
+                                  "fa2_fwd_ex", "fa2_fwd_fp8",
                                   "fa2_fwd_from_host",
                                   "fa2_fwd_noalloc", "fa2_fwd_window", "fa2_fwd_ws", "fa2_get_device_error",
                                   "fa2_status_string", "fa2_version", "fa2_workspace_size"]
@@ -231,3 +231,19 @@ def test_fwd_ex_validation(lib):
     assert call(causal=1, window=4, Lq=9, Lk=8) == INVALID        # and Lq <= Lk
     assert call(ws=P + 16) == INVALID                             # workspace not 256-byte aligned
     assert call(D=96) == UNSUPPORTED
+
+
+def test_fwd_fp8_validation(lib):
+    """fa2_fwd_fp8's host-side checks (no CUDA call is made for these): the descales are
+    required and 4-byte aligned, D must be 128, Lq == 0 is a no-op."""
+    P = 0x10000
+    f = lib.fa2_fwd_fp8
+    # q, k, v, dq, dk, dv, o, lse, B, H, Lq, Lk, D, causal, scale, ws, ws_bytes, stream
+    assert f(P, P, P, None, P, P, P, P, 1, 1, 8, 8, 128, 0, 0.1, None, 0, None) == INVALID
+    assert f(P, P, P, P, P + 2, P, P, P, 1, 1, 8, 8, 128, 0, 0.1, None, 0, None) == INVALID
+    assert f(P, P, P, P, P, None, P, P, 1, 1, 8, 8, 128, 0, 0.1, None, 0, None) == INVALID
+    assert f(P, P, P, P, P, P, P, P, 1, 1, 8, 8, 64, 0, 0.1, None, 0, None) == UNSUPPORTED
+    assert f(P, P, P, P, P, P, P, P, 1, 1, 8, 8, 96, 0, 0.1, None, 0, None) == UNSUPPORTED
+    assert f(P, P, P, P, P, P, P + 8, P, 1, 1, 8, 8, 128, 0, 0.1, None, 0, None) == INVALID   # o misaligned
+    assert f(P, P, P, P, P, P, P, P, 1, 1, 0, 8, 128, 0, 0.1, None, 0, None) == OK   # Lq == 0
+    assert f(P, P, P, P, P, P, P, P, 1, 1, 8, 8, 128, 0, float("nan"), None, 0, None) == INVALID

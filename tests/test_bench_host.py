@@ -60,9 +60,12 @@ def test_traffic_record_tracks_kernel_source(tmp_path, monkeypatch):
     rec = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if os.path.exists(rec):
         d = json.load(open(rec))
-        got = bench.load_traffic(digest)
-        assert (got is not None) == (d["kernel_source_digest"] == digest)
-    assert bench.load_traffic("not-a-digest") is None
+        for name in d.get("workloads", {}):
+            got = bench.load_traffic(digest, name)
+            assert (got is not None) == (d["kernel_source_digest"] == digest)
+            if got is not None:
+                assert got["dram_bytes_per_launch"] > 0
+    assert bench.load_traffic("not-a-digest", "c4") is None
 
 
 def test_reference_arm_prints_one_line():

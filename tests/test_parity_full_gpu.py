@@ -1,60 +1,83 @@
-"""CUDA path vs the fp64 oracle at the full workload sizes, in the launch
-configuration the benchmark times: c2 every element, c3/c4/c5 on sampled rows
-(tile edges of the first and last head plus random rows), and properties that
-hold at any size on every row (finite outputs, causal row 0 equals V_0)."""
-import math
-import zlib
+"""CUDA path vs the fp64 oracle at the full workload sizes, EVERY element.
 
-import numpy as np
+Each workload (B2 H16 L4096 D128 both modes, B1 H32 L16384 D128 causal,
+B2 H8 Lq2000 Lk3000 D256 peaky non-causal, B4 H16 L1024 D64 both modes) runs in
+the launch configuration the benchmark times and is compared element by element
+with the oracle's full output: plain ``fa2_fwd`` (whole query tiles), and for
+non-causal passes also the workspace path with the key-tile ranges cut at every
+SM boundary (``FA2_SPLIT=always``), whose part merges touch one query tile per
+cut.  The oracle's output for a workload is computed once and shared by its paths
+(about a minute of host time for the 16384-key causal workload).
+
+Definition: "Chapter 08: Flash Attention -- blocked attention", sections 3-4;
+Olowookere, "FlashAttention-2 from scratch with a custom Triton kernel", "The
+core idea".  Besides the tolerance check, each report carries the flat
+max|dO| over every element and how many elements exceed 1e-2 (the bf16
+half-spacing allowance for |O| >= 4 being the only way one may).
+"""
+import json
+import os
+
 import pytest
 import torch
 
 import oracle
 from io_aware_exact_fa2_gb300.workloads import WORKLOADS, workload_inputs
-from parity import compare, run_cuda, sample_rows
+from parity import compare, run_cuda
 
 pytestmark = pytest.mark.gpu
 
+# (workload, mode, path) in an order that lets one oracle result serve its paths
+CASES = [(name, mode, path)
+         for name in ("c2", "c3", "c5", "c4")
+         for mode in WORKLOADS[name].modes
+         for path in (("plain", "split") if mode == "noncausal" else ("plain",))]
 
-def _cases():
-    for name in ("c2", "c3", "c4", "c5"):
-        for mode in WORKLOADS[name].modes:
-            yield name, mode
+_REF = {}
 
 
-def _run_ws(q, k, v, causal, scale):
+def _reference(name, mode):
+    """Oracle O, LSE (fp64) and the inputs of one workload and mode, computed once."""
+    key = (name, mode)
+    if key not in _REF:
+        _REF.clear()   # keep one workload's reference in host memory at a time
+        w = WORKLOADS[name]
+        q, k, v = workload_inputs(w)
+        o_ref, lse_ref = oracle.attention(q, k, v, mode == "causal", w.scale)
+        _REF[key] = (q, k, v, o_ref, lse_ref)
+    return _REF[key]
+
+
+def _run_split(q, k, v, causal, scale):
     from io_aware_exact_fa2_gb300 import fa2_fwd, fa2_get_device_error, fa2_workspace
     dev = torch.device("cuda:0")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    fa2_fwd(qd, kd, vd, o, lse, causal, scale, workspace=fa2_workspace(qd, kd, causal))
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full(q.shape[:3], float("nan"), dtype=torch.float32, device=dev)
+    ws = fa2_workspace(qd, kd, causal)
+    assert ws is not None and ws.numel() > 0, "the forced split schedule takes a workspace"
+    fa2_fwd(qd, kd, vd, o, lse, causal, scale, workspace=ws)
     st, code = fa2_get_device_error()
-    assert st == 0, code
+    assert st == 0, f"device error {code:#x}"
     return o.cpu(), lse.cpu()
 
 
-@pytest.mark.parametrize("path", ["plain", "workspace"])
-@pytest.mark.parametrize("name,mode", list(_cases()))
-def test_full_size(name, mode, path, monkeypatch):
+@pytest.mark.parametrize("name,mode,path", CASES)
+def test_full_size_every_element(name, mode, path, monkeypatch):
     w = WORKLOADS[name]
     causal = mode == "causal"
-    if path == "workspace" and causal:
-        pytest.skip("causal passes do not use the workspace")
-    if path == "workspace":   # cut key-tile ranges even where the estimate would not
+    q, k, v, o_ref, lse_ref = _reference(name, mode)
+    if path == "split":
         monkeypatch.setenv("FA2_SPLIT", "always")
-    q, k, v = workload_inputs(w)
-    o, lse = (run_cuda if path == "plain" else _run_ws)(q, k, v, causal, w.scale)
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
-    if causal:
-        assert torch.equal(o[:, :, 0], v[:, :, 0])
-    if name == "c2":
-        o_ref, lse_ref = oracle.attention(q, k, v, causal, w.scale)
-        rep = compare(o, lse, o_ref, lse_ref)
+        o, lse = _run_split(q, k, v, causal, w.scale)
     else:
-        rows = sample_rows(w.B, w.H, w.Lq, n_random=1024, seed=zlib.crc32((name + mode).encode()))
-        o_ref, lse_ref = oracle.attention_rows(q, k, v, causal, w.scale, rows)
-        o_s = o.reshape(-1, w.D)[torch.from_numpy(rows)]
-        l_s = lse.reshape(-1)[torch.from_numpy(rows)]
-        rep = compare(o_s, l_s, o_ref, lse_ref)
-    print(f"{name} {mode} {path}: {rep}")
+        o, lse = run_cuda(q, k, v, causal, w.scale)
+    if causal:   # row 0 sees key 0 alone: O_0 = V_0 exactly
+        assert torch.equal(o[:, :, 0], v[:, :, 0])
+    rep = compare(o, lse, o_ref, lse_ref)
+    rep.update(workload=name, mode=mode, path=path)
+    print(json.dumps(rep))
+    out = os.environ.get("FA2_PARITY_REPORT")
+    if out:   # one JSON line per case, for the measured error table
+        with open(out, "a") as fh:
+            fh.write(json.dumps(rep) + "\n")

@@ -19,11 +19,9 @@ pytestmark = pytest.mark.gpu
 VARIANTS = {
     "d64_nq1_cs2_ks4": (64, ["-DFA2_D64_NQ=1", "-DFA2_D64_KS=4", "-DFA2_D64_CS=2"]),
     "d128_nq1_cs2": (128, ["-DFA2_D128_NQ=1", "-DFA2_D128_CS=2"]),
-    "d128_nq2_cs2": (128, ["-DFA2_D128_CS=2"]),
     # Q kept in TMEM (two buffers at D = 128, one at D = 256, which is that size's default)
     "d128_nq1_qt": (128, ["-DFA2_D128_NQ=1", "-DFA2_D128_QT=1"]),
     "d128_nq1_cs2_qt": (128, ["-DFA2_D128_NQ=1", "-DFA2_D128_CS=2", "-DFA2_D128_QT=1"]),
-    "d256_cs2": (256, ["-DFA2_D256_CS=2"]),
     "d256_q_in_smem": (256, ["-DFA2_D256_QT=0"]),
 }
 

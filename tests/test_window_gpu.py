@@ -1,22 +1,27 @@
 """Causal sliding-window forward ("Flash Attention: principles and implementation",
 section 6.3: window_size = (w, 0) with causal) on the GPU against the oracle.
 
-Tolerance, from the arithmetic.  The kernel weighs the values with bf16-rounded
+Tolerance.  Every row that sees at least 64 keys meets the forward workloads'
+rule (max|dO| <= 1e-2, plus half a bf16 spacing where |O| >= 4; max|dLSE| <=
+1e-3), the same bar the unwindowed kernel meets.  Only rows with fewer visible
+keys -- where a narrow window leaves a handful (w = 1: two) -- take a bound
+derived from the arithmetic: the kernel weighs the values with bf16-rounded
 probabilities p~_j = p_j (1 + e_j), |e_j| <= 2^-9, and divides by their sum, so
 each normalised weight moves by at most ~2^-8 of itself and
 |dO_id| <= 2^-8 * max_{j visible} |v_jd - O_id|; storing O in bf16 adds up to
-2^-9 |O_id|.  With thousands of keys per row the errors average out far below
-the forward workloads' 1e-2, but a narrow window leaves only a few keys per row
-(w = 1: two), where the bound itself exceeds 1e-2.  So every element must meet
-|dO| <= 2^-8 * max_j |v_jd - O_id| + 2^-8 |O_id| + 1e-5, and LSE the forward's
-1e-3."""
+2^-9 |O_id|.  With few keys the errors do not average out and that bound can
+exceed 1e-2 (measured: one element at 1.016e-2 with |O| = 2.16 for w = 1).
+LSE meets 1e-3 on every row."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from io_aware_exact_fa2_gb300.workloads import make_qkv
-from parity import sample_rows, scale_of
+from parity import o_tolerance, sample_rows, scale_of
+
+# rows that see at least this many keys are held to the forward's flat rule
+FLAT_RULE_MIN_KEYS = 64
 
 pytestmark = pytest.mark.gpu
 
@@ -34,13 +39,19 @@ def compare(o, lse, o_ref, lse_ref, v, window, Lq, rows=None):
         rows = np.arange(og.shape[0])
     assert np.isfinite(og).all() and np.isfinite(lg).all()
     assert np.max(np.abs(lg - lrf)) <= 1e-3
+    n_flat = 0
     for n, r in enumerate(rows):
         bh, i = divmod(int(r), Lq)
         lo, hi = max(0, i - window), min(i, Lk - 1)
-        spread = np.max(np.abs(vf[bh, lo:hi + 1] - orf[n]), axis=0)
-        bound = 2.0 ** -8 * spread + 2.0 ** -8 * np.abs(orf[n]) + 1e-5
         err = np.abs(og[n] - orf[n])
-        assert np.all(err <= bound), (int(r), float(np.max(err - bound)))
+        if hi - lo + 1 >= FLAT_RULE_MIN_KEYS:
+            bound = o_tolerance(orf[n])
+            n_flat += 1
+        else:
+            spread = np.max(np.abs(vf[bh, lo:hi + 1] - orf[n]), axis=0)
+            bound = 2.0 ** -8 * spread + 2.0 ** -8 * np.abs(orf[n]) + 1e-5
+        assert np.all(err <= bound), (int(r), hi - lo + 1, float(np.max(err - bound)))
+    return n_flat
 
 
 def run_window(q, k, v, window, scale):
@@ -64,7 +75,9 @@ def test_window_every_element(D, window):
     q, k, v = make_qkv(2, 2, 600, 600, D, seed_base=9000 + D + window)
     o, lse = run_window(q, k, v, window, scale_of(D))
     o_ref, lse_ref = oracle.attention(q, k, v, True, scale_of(D), window=window)
-    compare(o, lse, o_ref, lse_ref, v, window, 600)
+    n_flat = compare(o, lse, o_ref, lse_ref, v, window, 600)
+    if window >= FLAT_RULE_MIN_KEYS:   # most rows see >= 64 keys: they met the flat rule
+        assert n_flat >= 2 * 2 * (600 - FLAT_RULE_MIN_KEYS)
 
 
 @pytest.mark.parametrize("Lq,Lk", [(300, 457), (1, 9), (129, 130)])
@@ -91,5 +104,6 @@ def test_window_at_the_forward_bench_size():
     rows = sample_rows(B, H, L, n_random=512, seed=9301)
     o_ref, lse_ref = oracle.attention_rows(q, k, v, True, scale_of(D), rows, window=w)
     idx = torch.from_numpy(rows)
-    compare(o.reshape(-1, D)[idx], lse.reshape(-1)[idx], o_ref, lse_ref, v, w, L, rows=rows)
+    n_flat = compare(o.reshape(-1, D)[idx], lse.reshape(-1)[idx], o_ref, lse_ref, v, w, L, rows=rows)
+    assert n_flat >= 0.9 * len(rows)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()

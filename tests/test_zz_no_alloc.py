@@ -47,22 +47,25 @@ def test_noalloc_rejects_bad_arguments_on_the_host(binding):
     assert f(P, P, P, P, P, 1, 1, 0, 8, 64, 0, 0.125, None) == 0   # Lq == 0: no-op
 
 
-# (B, H, Lq, Lk, D, causal): cut-range schedule for each D, one shape the cost
-# model runs as whole tiles (no scratch used), and a causal pass
+# (B, H, Lq, Lk, D, causal, uses_scratch): the cut-range schedule for each D (it
+# takes the scratch), one non-causal shape whose whole query tiles already fill the
+# 152 SMs evenly (152 units of 8 key tiles: the cost model keeps whole units, no
+# scratch), and a causal pass (never cut, no scratch)
 CASES = [
-    (1, 1, 1000, 4096, 128, False),
-    (1, 1, 1000, 4096, 64, False),
-    (1, 2, 700, 3000, 256, False),
-    (2, 16, 4096, 4096, 128, False),
-    (2, 3, 640, 1000, 128, False),
-    (1, 2, 900, 900, 128, True),
+    (1, 1, 1000, 4096, 128, False, True),
+    (1, 1, 1000, 4096, 64, False, True),
+    (1, 2, 700, 3000, 256, False, True),
+    (2, 16, 4096, 4096, 128, False, True),
+    (2, 3, 640, 1000, 128, False, True),
+    (2, 76, 256, 1024, 64, False, False),
+    (1, 2, 900, 900, 128, True, False),
 ]
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dLq%dLk%dD%d%s" % (c[:5] + ("c" if c[5] else "",)))
 def test_noalloc_matches_workspace_entry_point_twice(binding, case):
-    B, H, Lq, Lk, D, causal = case
+    B, H, Lq, Lk, D, causal, uses_scratch = case
     dev = torch.device("cuda:0")
     scale = D ** -0.5
     inputs = [tuple(t.to(dev) for t in make_qkv(B, H, Lq, Lk, D, seed_base=7000 + 10 * D + s))
@@ -75,6 +78,9 @@ def test_noalloc_matches_workspace_entry_point_twice(binding, case):
         refs.append((o, lse))
     need = binding.fa2_workspace_size(B, H, Lq, Lk, D, causal)
     assert need <= binding.NOALLOC_SCRATCH_BYTES
+    # the case takes the path it is meant to cover: cut ranges through the scratch,
+    # or whole query tiles without it
+    assert (need > 0) == uses_scratch, need
 
     outs = [(torch.full((B, H, Lq, D), float("nan"), dtype=torch.bfloat16, device=dev),
              torch.full((B, H, Lq), float("nan"), dtype=torch.float32, device=dev)) for _ in inputs]
@@ -100,6 +106,7 @@ def test_noalloc_back_to_back_on_one_stream(binding):
     one stream, so they share the scratch safely) match the workspace entry point."""
     B, H, Lq, Lk, D = 1, 1, 1000, 4096, 128
     dev = torch.device("cuda:0")
+    assert binding.fa2_workspace_size(B, H, Lq, Lk, D, False) > 0   # the cut-range path
     q, k, v = (t.to(dev) for t in make_qkv(B, H, Lq, Lk, D, seed_base=7500))
     o_ref = torch.empty(B, H, Lq, D, dtype=torch.bfloat16, device=dev)
     lse_ref = torch.empty(B, H, Lq, dtype=torch.float32, device=dev)
