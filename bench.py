@@ -224,7 +224,7 @@ FWD_KERNEL_LABEL = {64: "fa2::fwd_kernel<D=64,BN=128,NQ=2>", 128: "fa2::fwd_kern
 # the other workloads, timed beside the headline in the same run (context, not the headline)
 PER_CONFIG = [("c3", "noncausal"), ("c3", "causal"), ("c2", "noncausal"), ("c2", "causal"),
               ("c5", "noncausal"), ("c4", "causal")]
-BWD_DIMS = (64, 128)
+BWD_DIMS = (64, 128, 256)
 # the e4m3 forward (fa2_fwd_fp8) on the D = 128 workloads' shapes; its peak is the measured
 # bf16 peak times the nominal fp8 / bf16 dense ratio (4.5 / 2.25 PFLOP/s)
 FP8_CONFIG = [("c3", "noncausal"), ("c3", "causal"), ("c4", "causal")]

@@ -353,8 +353,8 @@ FA2_EXPORT fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *
         scratch = fa2::noalloc_scratch_ptr(dev);
         if (!scratch)
             return FA2_ERR_CUDA;
-        // the arrival counters (one int per CTA and Q tile, at most 2 Q tiles) start at zero
-        const size_t zero_bytes = fa2::align256(static_cast<size_t>(sms) * 2 * sizeof(int));
+        // the arrival counters (one int per CTA and Q tile, at most 4 Q tiles) start at zero
+        const size_t zero_bytes = fa2::align256(static_cast<size_t>(sms) * 4 * sizeof(int));
         if (cudaMemsetAsync(scratch, 0, zero_bytes < need ? zero_bytes : need, static_cast<cudaStream_t>(stream)) !=
             cudaSuccess) {
             (void)cudaGetLastError();
@@ -372,7 +372,7 @@ FA2_EXPORT fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D
     *bytes = 0;
     if (B <= 0 || H <= 0 || Lq < 0 || Lk <= 0 || D <= 0 || static_cast<long long>(B) * H > INT_MAX)
         return FA2_ERR_INVALID_ARG;
-    if (D != 64 && D != 128)
+    if (D != 64 && D != 128 && D != 256)
         return FA2_ERR_UNSUPPORTED;
     *bytes = fa2::align256(fa2::bwd_stats_bytes(B, H, Lq));
     return FA2_OK;
@@ -405,8 +405,6 @@ fa2_status bwd(const void *q, const void *k, const void *v, const void *o, const
     fa2_status st = fa2::validate(q, k, v, o, lse, B, H, Lq, Lk, D, scale);
     if (st != FA2_OK)
         return st;
-    if (D != 64 && D != 128)
-        return FA2_ERR_UNSUPPORTED;
     if (!dout || !dq || !dk || !dv || (!workspace && Lq > 0))
         return FA2_ERR_INVALID_ARG;
     if (!fa2::aligned(dout, 16) || !fa2::aligned(dq, 16) || !fa2::aligned(dk, 16) || !fa2::aligned(dv, 16) ||

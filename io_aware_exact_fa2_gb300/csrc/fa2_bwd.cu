@@ -13,10 +13,15 @@ namespace fa2 {
 // dQ: 128 queries resident, key tiles of 64 through a 4-stage ring.  Two score
 // buffer pairs let one step's MMAs run while the previous step's elementwise
 // work finishes.
+//
+// D = 256: two CTAs per resident tile, each accumulating 128 of the 256 gradient
+// columns (both compute the step's full score products), and a one-stage ring: the
+// resident tiles (2 x 64 KB) and one stage of streamed tiles (2 x 32 KB) fill shared
+// memory; the dQ kernel's score products read Q and dO from shared memory.
 template <int D>
-using BwdKV = BwdCfg<D, 128, 64, 4, 8>;
+using BwdKV = BwdCfg<D, 128, 64, (D == 256 ? 1 : 4), 8, (D == 256 ? 128 : D)>;
 template <int D>
-using BwdQ = BwdCfg<D, 128, 64, 4, 8>;
+using BwdQ = BwdCfg<D, 128, 64, (D == 256 ? 1 : 4), 8, (D == 256 ? 128 : D)>;
 static_assert(BWD_STAT_TILE_ROWS == BWD_STAT_ROWS, "workspace sizing and kernels agree on the statistics tiles");
 
 template <class K>
@@ -122,12 +127,12 @@ static fa2_status launch_bwd_d(const BwdArgs &a)
             static_cast<const uint16_t *>(a.o), static_cast<const uint16_t *>(a.dout), a.lse, a.stats, a.Lq,
             n_stat_tiles, rows, a.H, BwdRowStrides{a.so.b, a.so.h, a.so.l}, BwdRowStrides{a.sdo.b, a.sdo.h, a.sdo.l});
         const long long n_qt = (a.Lq + CQ::RES - 1) / CQ::RES;
-        fa2_bwd_q_kernel<CQ><<<static_cast<unsigned>(n_qt * BH), CQ::NUM_THREADS, CQ::SMEM_BYTES, a.stream>>>(
-            q_res, do_res, k_str, v_str, p);
+        fa2_bwd_q_kernel<CQ><<<static_cast<unsigned>(n_qt * BH * CQ::NH), CQ::NUM_THREADS, CQ::SMEM_BYTES,
+                               a.stream>>>(q_res, do_res, k_str, v_str, p);
     }
     const long long n_kt = (a.Lk + CKV::RES - 1) / CKV::RES;
-    fa2_bwd_kv_kernel<CKV><<<static_cast<unsigned>(n_kt * BH), CKV::NUM_THREADS, CKV::SMEM_BYTES, a.stream>>>(
-        k_res, v_res, q_str, do_str, p);
+    fa2_bwd_kv_kernel<CKV><<<static_cast<unsigned>(n_kt * BH * CKV::NH), CKV::NUM_THREADS, CKV::SMEM_BYTES,
+                             a.stream>>>(k_res, v_res, q_str, do_str, p);
     return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
@@ -136,6 +141,7 @@ fa2_status launch_bwd(const BwdArgs &a)
     switch (a.D) {
     case 64: return launch_bwd_d<64>(a);
     case 128: return launch_bwd_d<128>(a);
+    case 256: return launch_bwd_d<256>(a);
     default: return FA2_ERR_UNSUPPORTED;
     }
 }

@@ -157,14 +157,25 @@ __global__ void __launch_bounds__(BWD_DELTA_THREADS) fa2_bwd_delta_kernel(const 
 // Shared configuration of the two gradient kernels: RES rows of the resident
 // tiles (TMEM lanes), STR rows per streamed tile, head dimension D, EW
 // elementwise warps (4: one per 32-lane TMEM quarter; 8: two per quarter, each
-// with half of a step's columns).
-template <int D_, int RES_, int STR_, int RING_, int EW_>
+// with half of a step's columns), DH gradient columns per CTA.  With DH = D / 2
+// (D = 256) two CTAs share each resident tile: both compute the step's full-D
+// score products, each accumulates and stores one half of the gradient columns,
+// so that the gradient accumulators and the score buffers fit the 512 TMEM columns.
+template <int D_, int RES_, int STR_, int RING_, int EW_, int DH_ = D_>
 struct BwdCfg {
     static constexpr int D = D_;
     static constexpr int RES = RES_;     // resident rows per CTA (= 128 TMEM lanes)
     static constexpr int STR = STR_;     // rows of a streamed tile per step
     static constexpr int RING = RING_;   // streamed-tile ring stages
     static constexpr int EW = EW_;       // elementwise warps
+    static constexpr int DH = DH_;       // gradient columns this CTA accumulates
+    static constexpr int NH = D / DH;    // CTAs per resident tile (one per column half)
+    // score pairs issued ahead of the gradient MMAs: two buffer pairs, but never more
+    // than the ring holds (a pair waits for its stage's tiles)
+    static constexpr int LA = RING >= 2 ? 2 : 1;
+    // the dQ kernel keeps Q and dO as TMEM A operands where TMEM has room (D <= 128);
+    // otherwise its score products read them from shared memory
+    static constexpr bool RES_IN_TMEM = D <= 128;
     static constexpr int DB = D / 64;    // 64-column (128-byte) swizzle blocks
     static constexpr int RES_BLOCK = RES * 128;
     static constexpr int RES_TILE = DB * RES_BLOCK;
@@ -194,8 +205,9 @@ struct BwdCfg {
     static constexpr int WARP_PRODUCER = EW;
     static constexpr int WARP_MMA = EW + 1;
     static constexpr uint32_t IDESC_PAIR = ptx::idesc_bf16_f32(RES, STR, false, false);
-    static constexpr uint32_t IDESC_GRAD = ptx::idesc_bf16_f32(RES, D, false, true);
-    static_assert(D == 64 || D == 128, "gradient kernels support D = 64 and 128");
+    static constexpr uint32_t IDESC_GRAD = ptx::idesc_bf16_f32(RES, DH, false, true);
+    static_assert(D == 64 || D == 128 || D == 256, "gradient kernels support D = 64, 128 and 256");
+    static_assert(DH == D || (D == 256 && DH == 128), "the gradient columns are split in two at D = 256 only");
     static_assert(RES == 128 && STR % 16 == 0 && STR >= 32 && STR <= 128, "tile shape");
     static_assert(EW == 4 || EW == 8, "one or two elementwise warps per TMEM lane quarter");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
@@ -276,7 +288,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     using namespace ptx;
     static_assert(C::STR == BWD_STAT_ROWS, "one statistics tile per streamed query tile");
     static_assert(C::EW == 8 && C::STR == 64, "two elementwise warps of 32 query columns per lane quarter");
-    constexpr int TM_DV = 0, TM_DK = C::D, TM_ST = 2 * C::D, TM_DPT = 2 * C::D + 2 * C::STR;
+    constexpr int TM_DV = 0, TM_DK = C::DH, TM_ST = 2 * C::DH, TM_DPT = 2 * C::DH + 2 * C::STR;
     constexpr int TMEM_COLS = 512;
     static_assert(TM_DPT + 2 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
     extern __shared__ uint8_t smem_raw[];
@@ -291,8 +303,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // the most queries).  Otherwise head by head, so the CTAs running at one time stream
     // the same few heads' Q and dO through L2.
     const int n_kt = (p.Lk + C::RES - 1) / C::RES;
+    const int dh = static_cast<int>(blockIdx.x) % C::NH;   // this CTA's half of the gradient columns
     int kt, bh;
-    bwd_cta_tile(static_cast<int>(blockIdx.x), n_kt, p, kt, bh);
+    bwd_cta_tile(static_cast<int>(blockIdx.x) / C::NH, n_kt, p, kt, bh);
     if (kt >= n_kt)
         return;
     const int hh = bh % p.H, hb = bh / p.H;   // head and batch of this CTA's tiles
@@ -394,10 +407,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (n_steps > 0) {
                 const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
                 const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
-                // the same streamed tiles as MN-major B operands (N = D along the rows'
-                // 128-byte lines, K = query rows)
-                const uint64_t desc_q_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
-                const uint64_t desc_do_mn = sdesc_sw128(sbase + C::OFF_STR1, C::STR_BLOCK, 1024);
+                // the same streamed tiles as MN-major B operands (N = this CTA's DH columns
+                // along the rows' 128-byte lines, K = query rows)
+                const uint32_t half_off = dh * (C::DH / 64) * C::STR_BLOCK;
+                const uint64_t desc_q_mn = sdesc_sw128(sbase + C::OFF_STR0 + half_off, C::STR_BLOCK, 1024);
+                const uint64_t desc_do_mn = sdesc_sw128(sbase + C::OFF_STR1 + half_off, C::STR_BLOCK, 1024);
                 // the resident K and V tiles as K-major A operands
                 const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
                 const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
@@ -445,14 +459,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     mma_commit(bar(C::BAR_STR_EMPTY + st));   // this step's Q, dO and stats are free
                     return true;
                 };
-                if (ok)
-                    ok = issue_pair(0);
-                if (ok && n_steps > 1)
-                    ok = issue_pair(1);
+                for (int s = 0; s < C::LA && s < n_steps && ok; ++s)
+                    ok = issue_pair(s);
                 for (int s = 0; s < n_steps && ok; ++s) {
                     ok = issue_grad(s);
-                    if (ok && s + 2 < n_steps)
-                        ok = issue_pair(s + 2);   // into the buffers issue_grad(s) just read
+                    if (ok && s + C::LA < n_steps)
+                        ok = issue_pair(s + C::LA);   // into the buffers issue_grad(s + LA - 2) read
                 }
                 mma_commit(bar(C::BAR_DONE));
                 lone_wait(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 4, p.wait_limit_ns);
@@ -548,16 +560,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         // these keys
         const bool valid = kj < p.Lk;
         const long long ob = hb, oh = hh, orow = valid ? kj : 0;
-        uint16_t *out_row = half ? p.dk + ob * p.dk_sb + oh * p.dk_sh + orow * p.dk_sl
-                                 : p.dv + ob * p.dv_sb + oh * p.dv_sh + orow * p.dv_sl;
+        uint16_t *out_row = (half ? p.dk + ob * p.dk_sb + oh * p.dk_sh + orow * p.dk_sl
+                                  : p.dv + ob * p.dv_sb + oh * p.dv_sh + orow * p.dv_sl) + dh * C::DH;
         if (n_steps == 0) {
             if (valid) {
-                for (int d = 0; d < C::D; d += 8)
+                for (int d = 0; d < C::DH; d += 8)
                     *reinterpret_cast<uint4 *>(out_row + d) = make_uint4(0, 0, 0, 0);
             }
         } else if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 2, p.wait_limit_ns)) {
             tc_fence_after();
-            store_acc_row<C::D>(tmem + lane_base + (half ? TM_DK : TM_DV), half ? p.scale : 1.f, out_row, valid);
+            store_acc_row<C::DH>(tmem + lane_base + (half ? TM_DK : TM_DV), half ? p.scale : 1.f, out_row, valid);
         }
     }
 
@@ -585,10 +597,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // Q and dO are also copied into TMEM (TM_QA, TM_DOA) so that S = Q K^T and
     // dP = dO V^T read their A operand from TMEM instead of loading it from shared
     // memory for every instruction
-    constexpr int TM_DQ = 0, TM_S = C::D, TM_DP = C::D + 2 * C::STR;
-    constexpr int TM_QA = C::D + 4 * C::STR, TM_DOA = TM_QA + C::D / 2;
+    constexpr int TM_DQ = 0, TM_S = C::DH, TM_DP = C::DH + 2 * C::STR;
+    constexpr int TM_QA = C::DH + 4 * C::STR, TM_DOA = TM_QA + C::D / 2;   // RES_IN_TMEM only
     constexpr int TMEM_COLS = 512;
-    static_assert(TM_DOA + C::D / 2 <= TMEM_COLS, "TMEM budget exceeded");
+    static_assert((C::RES_IN_TMEM ? TM_DOA + C::D / 2 : TM_QA) <= TMEM_COLS, "TMEM budget exceeded");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -600,8 +612,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // last (heaviest) first.  Otherwise head by head, so the CTAs running at one time
     // stream the same few heads' K and V through L2.
     const int n_qt = (p.Lq + C::RES - 1) / C::RES;
+    const int dh = static_cast<int>(blockIdx.x) % C::NH;   // this CTA's half of dQ's columns
     int qt, bh;
-    bwd_cta_tile(static_cast<int>(blockIdx.x), n_qt, p, qt, bh);
+    bwd_cta_tile(static_cast<int>(blockIdx.x) / C::NH, n_qt, p, qt, bh);
     if (p.causal)
         qt = n_qt - 1 - qt;
     if (qt < 0)
@@ -688,9 +701,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         if (elect_one()) {
             const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_STR0, 16, 1024);
             const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_STR1, 16, 1024);
-            const uint64_t desc_k_mn = sdesc_sw128(sbase + C::OFF_STR0, C::STR_BLOCK, 1024);
-            // Q and dO copied into TMEM by the elementwise warps
-            bool ok = lone_wait(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
+            const uint64_t desc_k_mn =
+                sdesc_sw128(sbase + C::OFF_STR0 + dh * (C::DH / 64) * C::STR_BLOCK, C::STR_BLOCK, 1024);
+            // the resident Q and dO tiles as K-major A operands (when they stay in shared memory)
+            const uint64_t desc_q = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
+            const uint64_t desc_do = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
+            // Q and dO copied into TMEM by the elementwise warps, or landed in shared memory
+            bool ok = C::RES_IN_TMEM ? lone_wait(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns)
+                                     : lone_wait(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_MMA | 5, p.wait_limit_ns);
             tc_fence_after();
             const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
             // S(b) = Q K^T for step s, once the step's tiles have landed
@@ -703,8 +721,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < C::D / 16; ++kk) {
                     const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                    mma_ts(tmem + TM_S + b * C::STR, tmem + TM_QA + kk * 8, desc_k + stage_off(st) + to,
-                           C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                    if constexpr (C::RES_IN_TMEM)
+                        mma_ts(tmem + TM_S + b * C::STR, tmem + TM_QA + kk * 8, desc_k + stage_off(st) + to,
+                               C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss(tmem + TM_S + b * C::STR,
+                               desc_q + static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4),
+                               desc_k + stage_off(st) + to, C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::BAR_SCORE_FULL + b));
                 return true;
@@ -715,8 +738,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < C::D / 16; ++kk) {
                     const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                    mma_ts(tmem + TM_DP + b * C::STR, tmem + TM_DOA + kk * 8, desc_v + stage_off(st) + to,
-                           C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                    if constexpr (C::RES_IN_TMEM)
+                        mma_ts(tmem + TM_DP + b * C::STR, tmem + TM_DOA + kk * 8, desc_v + stage_off(st) + to,
+                               C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                    else
+                        mma_ss(tmem + TM_DP + b * C::STR,
+                               desc_do + static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4),
+                               desc_v + stage_off(st) + to, C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(C::BAR_DP_FULL + b));
             };
@@ -740,20 +768,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             };
             // S and dP are committed separately so that the elementwise warps start on
             // the exponentials while dP is still being computed
-            if (ok)
-                ok = issue_s(0);
-            if (ok)
-                issue_dp(0);
-            if (ok && n_steps > 1)
-                ok = issue_s(1);
-            if (ok && n_steps > 1)
-                issue_dp(1);
+            for (int s = 0; s < C::LA && s < n_steps && ok; ++s) {
+                ok = issue_s(s);
+                if (ok)
+                    issue_dp(s);
+            }
             for (int s = 0; s < n_steps && ok; ++s) {
                 ok = issue_grad(s);
-                if (ok && s + 2 < n_steps)
-                    ok = issue_s(s + 2);
-                if (ok && s + 2 < n_steps)
-                    issue_dp(s + 2);
+                if (ok && s + C::LA < n_steps)
+                    ok = issue_s(s + C::LA);
+                if (ok && s + C::LA < n_steps)
+                    issue_dp(s + C::LA);
             }
             mma_commit(bar(C::BAR_DONE));
             lone_wait(bar(C::BAR_DONE), 0, p.err, ERR_BWD_MMA | 8, p.wait_limit_ns);
@@ -779,8 +804,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const int lim = p.causal ? min(qi + 1, p.Lk) : p.Lk;
         const int lo = p.window >= 0 ? qi - p.window : 0;
         // this row of Q (half 0) or of dO (half 1) into TMEM, as a score MMA's A operand
-        bool ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
-        if (ok) {
+        bool ok = !C::RES_IN_TMEM || warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
+        if (ok && C::RES_IN_TMEM) {
             if (half == 0)
                 copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_QA);
             else
@@ -855,14 +880,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (lane == 0)
                 mbar_arrive(bar(C::BAR_GRAD_READY + b));
         }
-        // epilogue: scale * dQ, columns [half * D/2, (half + 1) * D/2) of this row
+        // epilogue: scale * dQ, columns dh * DH + [half * DH/2, (half + 1) * DH/2) of this row
         if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 4, p.wait_limit_ns)) {
             tc_fence_after();
-            store_acc_row<C::D / 2>(tmem + lane_base + TM_DQ + half * (C::D / 2), p.scale,
-                                    p.dq + static_cast<long long>(hb) * p.dq_sb +
-                                        static_cast<long long>(hh) * p.dq_sh +
-                                        static_cast<long long>(live ? qi : 0) * p.dq_sl + half * (C::D / 2),
-                                    live);
+            store_acc_row<C::DH / 2>(tmem + lane_base + TM_DQ + half * (C::DH / 2), p.scale,
+                                     p.dq + static_cast<long long>(hb) * p.dq_sb +
+                                         static_cast<long long>(hh) * p.dq_sh +
+                                         static_cast<long long>(live ? qi : 0) * p.dq_sl + dh * C::DH +
+                                         half * (C::DH / 2),
+                                     live);
         }
     }
 

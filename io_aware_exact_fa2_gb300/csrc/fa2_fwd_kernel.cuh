@@ -102,12 +102,6 @@ enum : int {
     ERR_DRAIN = 0x400,
 };
 
-// Exponentials taken on the FMA pipe (exp2_poly_f32x2) instead of the MUFU: pairs
-// per 32 columns of a row's scores (0: all on the MUFU).
-#ifndef FA2_EXP2_EMU_PAIRS
-#define FA2_EXP2_EMU_PAIRS 0
-#endif
-
 // Threshold (log2 units) above which a growing row max forces a rescale of O and l.
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.69314718055994530942f;
@@ -212,14 +206,23 @@ struct FwdCfg {
     static constexpr int NUM_SOFTMAX_WARPS = 4 * CS * NQ;
     static constexpr int WARP_PRODUCER = NUM_SOFTMAX_WARPS;
     static constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;
-    // With two softmax warpgroups the launch leaves 168 registers per thread; the
-    // control warpgroup drops to REG_CTRL and the softmax warpgroups rise to
-    // REG_SOFTMAX.  Budget: 2*128*200 + 128*104 = 64512 = 384 threads * 168.
-    static constexpr bool REG_SPLIT = (NUM_SOFTMAX_WARPS == 8);
-    static constexpr int REG_SOFTMAX = 200;
-    static constexpr int REG_CTRL = 104;
+    // With two or four softmax warpgroups the control warpgroup drops to REG_CTRL
+    // registers and the softmax warpgroups rise to REG_SOFTMAX, within what the launch
+    // gives the block (LAUNCH_REGS per thread, the most 65536 registers allow):
+    //   two:  384 threads * 168 = 64512 = 2*128*200 + 128*104
+    //   four: 640 threads *  96 = 61440 = 4*128*104 + 128*64
+    static constexpr bool REG_SPLIT = (NUM_SOFTMAX_WARPS == 8 || NUM_SOFTMAX_WARPS == 16);
+#ifndef FA2_REG16_SOFTMAX
+#define FA2_REG16_SOFTMAX 104
+#endif
+#ifndef FA2_REG16_CTRL
+#define FA2_REG16_CTRL 64
+#endif
+    static constexpr int REG_SOFTMAX = NUM_SOFTMAX_WARPS == 16 ? FA2_REG16_SOFTMAX : 200;
+    static constexpr int REG_CTRL = NUM_SOFTMAX_WARPS == 16 ? FA2_REG16_CTRL : 104;
     static constexpr int NUM_THREADS = 32 * (NUM_SOFTMAX_WARPS + (REG_SPLIT ? 4 : 2));
-    static_assert(!REG_SPLIT || 2 * 128 * REG_SOFTMAX + 128 * REG_CTRL <= NUM_THREADS * 168,
+    static constexpr int LAUNCH_REGS = (65536 / NUM_THREADS) / 8 * 8 > 255 ? 255 : (65536 / NUM_THREADS) / 8 * 8;
+    static_assert(!REG_SPLIT || NUM_SOFTMAX_WARPS * 32 * REG_SOFTMAX + 128 * REG_CTRL <= NUM_THREADS * LAUNCH_REGS,
                   "register split exceeds the launch allocation");
 
     static constexpr uint32_t IDESC_S =
@@ -229,7 +232,8 @@ struct FwdCfg {
 
     static_assert(D % 64 == 0 && D >= 64 && D <= 256, "D must be 64, 128 or 256");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64, 256]");
-    static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per work unit");
+    static_assert(NQ == 1 || NQ == 2 || NQ == 4, "one, two or four Q tiles per work unit");
+    static_assert(NQ <= 2 || CS == 1, "four Q tiles take one softmax warp per row");
     static_assert(CS == 1 || CS == 2, "one or two warps per row");
     static_assert(NS == 1 || NS == 2, "one or two S buffers per Q tile");
     static_assert(NCOL % 32 == 0 && OCOL % 32 == 0, "per-thread column slices are whole 32-column loads");
@@ -904,22 +908,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         float x0, x1, x2, x3;
                         unpack_f32x2(fma_f32x2(f32x2(s[c], s[c + 1]), c2x2, negm2), x0, x1);
                         unpack_f32x2(fma_f32x2(f32x2(s[c + 2], s[c + 3]), c2x2, negm2), x2, x3);
-                        float p0, p1, p2, p3;
-                        // the first FA2_EXP2_EMU_PAIRS column pairs of every 32 go to the FMA pipe
-                        // (c is a constant in each unrolled iteration, so the choice is static)
-                        const int pair = (c % 32) / 2;
-                        if (pair < FA2_EXP2_EMU_PAIRS) {
-                            unpack_f32x2(exp2_poly_f32x2(x0, x1), p0, p1);
-                        } else {
-                            p0 = ex2_approx(x0);
-                            p1 = ex2_approx(x1);
-                        }
-                        if (pair + 1 < FA2_EXP2_EMU_PAIRS) {
-                            unpack_f32x2(exp2_poly_f32x2(x2, x3), p2, p3);
-                        } else {
-                            p2 = ex2_approx(x2);
-                            p3 = ex2_approx(x3);
-                        }
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        const float p2 = ex2_approx(x2);
+                        const float p3 = ex2_approx(x3);
                         ls01 = add_f32x2(ls01, f32x2(p0, p1));
                         ls23 = add_f32x2(ls23, f32x2(p2, p3));
                         if constexpr (C::F8) {

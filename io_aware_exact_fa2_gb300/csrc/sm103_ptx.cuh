@@ -514,34 +514,6 @@ __device__ __forceinline__ uint64_t widen_bf16x2(uint32_t w)
     return static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xffff0000u) << 32);
 }
 
-// 2^x for a pair of fp32 x <= 128 on the FMA and integer pipes instead of the MUFU
-// (Cody-Waite range reduction x = n + f, n = floor(x), f in [0, 1), then 2^f from a
-// degree-3 polynomial and 2^n added into the exponent field).  The coefficients are
-// the relative-error minimax fit of 2^f on [0, 1] from the Remez exchange algorithm:
-// |p(f) / 2^f - 1| <= 7.5e-5 (bf16 weights round at 2^-9).  x is clamped below at
-// -126 (the smallest exponent the field add cannot wrap), so masked entries (-inf)
-// give about 2^-126 instead of 0.
-__device__ __forceinline__ uint64_t exp2_poly_f32x2(float x0, float x1)
-{
-    constexpr float SHIFT = 12582912.0f;   // 1.5 * 2^23: adding it (rounding down) leaves floor(x) in the low bits
-    const uint64_t x = f32x2(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-    uint64_t y, n, f, p;
-    const uint64_t sh = f32x2(SHIFT, SHIFT);
-    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(sh));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(n) : "l"(y), "l"(sh));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(f) : "l"(x), "l"(n));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(f), "l"(f32x2(0.07802452f, 0.07802452f)),
-        "l"(f32x2(0.22606716f, 0.22606716f)));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(p), "l"(f), "l"(f32x2(0.69583356f, 0.69583356f)));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p) : "l"(p), "l"(f), "l"(f32x2(0.99992520f, 0.99992520f)));
-    // floor(x) sits in the low bits of y's pattern (two's complement over the low 9
-    // bits); shifted into the exponent field it scales p(f) by 2^n
-    const uint32_t ylo = static_cast<uint32_t>(y), yhi = static_cast<uint32_t>(y >> 32);
-    const uint32_t plo = static_cast<uint32_t>(p) + (ylo << 23);
-    const uint32_t phi = static_cast<uint32_t>(p >> 32) + (yhi << 23);
-    return static_cast<uint64_t>(plo) | (static_cast<uint64_t>(phi) << 32);
-}
-
 // Four fp32 -> four e4m3 in one word (round to nearest even, saturating at +-448),
 // a0 in bits [0,8) ... a3 in bits [24,32).
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3)

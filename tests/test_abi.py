@@ -148,7 +148,8 @@ def test_bwd_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.fa2_bwd_workspace_size(2, 3, 100, 50, 128, ctypes.byref(n)) == OK
     assert n.value == 2 * 3 * 128 * 2 * 4   # (-lse2, -Delta) per row, 100 rows padded to 128
-    assert lib.fa2_bwd_workspace_size(2, 3, 100, 50, 256, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.fa2_bwd_workspace_size(2, 3, 100, 50, 256, ctypes.byref(n)) == OK and n.value == 2 * 3 * 128 * 2 * 4
+    assert lib.fa2_bwd_workspace_size(2, 3, 100, 50, 96, ctypes.byref(n)) == UNSUPPORTED
     assert lib.fa2_bwd_workspace_size(0, 3, 100, 50, 64, ctypes.byref(n)) == INVALID
     f = lib.fa2_bwd
     good = dict(q=P, k=P, v=P, o=P, lse=P, do=P, dq=P, dk=P, dv=P, B=1, H=1, Lq=8, Lk=8, D=64, causal=0,
@@ -163,7 +164,7 @@ def test_bwd_validation(lib):
     assert call_bwd(dk=0) == INVALID
     assert call_bwd(ws=0) == INVALID
     assert call_bwd(ws_bytes=4) == INVALID
-    assert call_bwd(D=256) == UNSUPPORTED
+    assert call_bwd(D=96) == UNSUPPORTED
     assert call_bwd(scale=float("nan")) == INVALID
 
 
@@ -178,7 +179,7 @@ def test_bwd_window_validation(lib):
     assert call(Lq=9) == INVALID
     assert call(do=0) == INVALID
     assert call(ws_bytes=4) == INVALID
-    assert call(D=256) == UNSUPPORTED
+    assert call(D=96) == UNSUPPORTED
 
 
 def test_bwd_ex_validation(lib):

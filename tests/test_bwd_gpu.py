@@ -63,14 +63,14 @@ def compare_grads(inputs, got, causal, heads=None):
     return report
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
 def test_c1_every_element(D, causal):
     inputs, got = run_bwd(1, 2, 128, 128, D, causal, seed=5100 + D)
     compare_grads(inputs, got, causal)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
 def test_ragged_multi_tile(D, causal):
     """Lq, Lk not multiples of any tile (query tiles of 64 and 128, key tiles of 64 and 128)."""
@@ -112,12 +112,84 @@ def test_c3_size_sampled_heads(causal):
     compare_grads(inputs, got, causal, heads=[0, 31])
 
 
-def test_deterministic():
+@pytest.mark.parametrize("D", [128, 256])
+def test_deterministic(D):
     """No atomics: the same inputs give bit-identical gradients."""
-    _, a = run_bwd(2, 2, 333, 400, 128, True, seed=5600)
-    _, b = run_bwd(2, 2, 333, 400, 128, True, seed=5600)
+    _, a = run_bwd(2, 2, 333, 400, D, True, seed=5600)
+    _, b = run_bwd(2, 2, 333, 400, D, True, seed=5600)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def delta_term(q, k, v, do, o_stored, scale, heads):
+    """Relative rms, per gradient, of the error that Delta = rowsum(dO * O) takes from the
+    STORED (bf16) O ("Chapter 08: Flash Attention -- blocked attention", section 6.2
+    defines Delta from the forward's output): dDelta_i = sum_d dO_id (O~_id - O_id), and
+    dS = P (dP - Delta) passes -P dDelta on, so dQ errs by -scale dDelta (P K) and dK by
+    -scale (P dDelta)^T Q.  Where one key dominates a row, dP - Delta cancels and this
+    term is no longer small next to the bf16 operand rounding."""
+    import oracle as orc
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    dq, dk, _, _ = orc.gradients(q, k, v, do, False, scale, heads=heads)   # only their rms is used
+    o_exact, _ = orc.attention(q, k, v, False, scale)
+    out = ("dq", "dk")
+    Q, K, DO = (t.double().numpy().reshape(B * H, -1, D)[heads] for t in (q, k, do))
+    OE = o_exact.reshape(B * H, Lq, D)[heads]
+    OS = o_stored.double().numpy().reshape(B * H, Lq, D)[heads]
+    num = {"dq": 0.0, "dk": 0.0}
+    den = {"dq": 0.0, "dk": 0.0}
+    ref = {"dq": dq, "dk": dk}
+    for n in range(len(heads)):
+        s = scale * Q[n] @ K[n].T
+        P = np.exp(s - s.max(1, keepdims=True))
+        P /= P.sum(1, keepdims=True)
+        dd = (DO[n] * (OS[n] - OE[n])).sum(1)
+        e = {"dq": scale * dd[:, None] * (P @ K[n]), "dk": scale * (P * dd[:, None]).T @ Q[n]}
+        for g in out:
+            num[g] += np.sum(e[g] ** 2)
+            den[g] += np.sum(ref[g][n] ** 2)
+    return {g: float(np.sqrt(num[g] / den[g])) for g in out}
+
+
+def test_d256_peaky_workload_shape_sampled_heads():
+    """B2 H8 Lq2000 Lk3000 D256 with every 64th key row x8 (the peaky D = 256 workload):
+    every element of two heads.  At D = 256 two CTAs share each resident tile, each
+    accumulating one half of the gradient columns.
+
+    Tolerance: the module's bar is twice the bf16 operand/output rounding predicted for
+    N(0, 1) rows (~2.5e-3 rel rms).  Here each row has a dominant key, so the rounding
+    of the stored O inside Delta adds an error of its own (delta_term: about 4.5e-3 rel
+    rms for dq and dk on these heads, computed from the exact and stored O).  The bar
+    for dq and dk is twice the two combined, sqrt(2.5e-3^2 + term^2); dv (no Delta in
+    it) keeps the module's bar."""
+    from io_aware_exact_fa2_gb300 import fa2_bwd, fa2_fwd, fa2_get_device_error
+    from io_aware_exact_fa2_gb300.workloads import WORKLOADS, workload_inputs
+    w = WORKLOADS["c5"]
+    dev = torch.device("cuda:0")
+    q, k, v = workload_inputs(w)
+    do = make_qkv(w.B, w.H, w.Lq, w.Lq, w.D, seed_base=w.seed_base + 7)[0]
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty(w.B, w.H, w.Lq, w.D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.H, w.Lq, dtype=torch.float32, device=dev)
+    fa2_fwd(qd, kd, vd, o, lse, False, w.scale)
+    grads = [torch.full_like(t, float("nan")) for t in (qd, kd, vd)]
+    fa2_bwd(qd, kd, vd, o, lse, dod, *grads, False, w.scale)
+    st, code = fa2_get_device_error()
+    assert st == 0, f"device error {code:#x}"
+    heads = [0, 15]
+    term = delta_term(q, k, v, do, o.cpu(), w.scale, heads)
+    ref = oracle.gradients(q, k, v, do, False, w.scale, heads=heads)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref[:3]):
+        g = g.cpu().double().reshape(w.B * w.H, *g.shape[2:]).numpy()[heads]
+        assert np.isfinite(g).all(), name
+        err = np.abs(g - r)
+        rel_rms = np.sqrt(np.mean(err ** 2)) / np.sqrt(np.mean(r ** 2))
+        rel_max = err.max() / np.abs(r).max()
+        bar = 2 * np.hypot(2.5e-3, term[name]) if name in term else REL_RMS
+        print(f"c5 backward {name}: rel rms {rel_rms:.2e} (bar {bar:.2e}), rel max {rel_max:.2e}")
+        assert rel_rms <= bar, (name, rel_rms, bar)
+        assert rel_max <= REL_MAX, (name, rel_max)
 
 
 def test_no_queries_zero_key_gradients():
@@ -144,7 +216,7 @@ def test_no_queries_zero_key_gradients():
 def test_unsupported_head_dim():
     from io_aware_exact_fa2_gb300 import Fa2Error, fa2_bwd
     dev = torch.device("cuda:0")
-    t = torch.zeros(1, 1, 8, 256, dtype=torch.bfloat16, device=dev)
+    t = torch.zeros(1, 1, 8, 96, dtype=torch.bfloat16, device=dev)
     lse = torch.zeros(1, 1, 8, device=dev)
     with pytest.raises(Fa2Error):
         fa2_bwd(t, t, t, t, lse, t, torch.empty_like(t), torch.empty_like(t), torch.empty_like(t), False)

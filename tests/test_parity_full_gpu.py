@@ -17,6 +17,7 @@ half-spacing allowance for |O| >= 4 being the only way one may).
 """
 import json
 import os
+import time
 
 import pytest
 import torch
@@ -43,8 +44,9 @@ def _reference(name, mode):
         _REF.clear()   # keep one workload's reference in host memory at a time
         w = WORKLOADS[name]
         q, k, v = workload_inputs(w)
+        t0 = time.perf_counter()
         o_ref, lse_ref = oracle.attention(q, k, v, mode == "causal", w.scale)
-        _REF[key] = (q, k, v, o_ref, lse_ref)
+        _REF[key] = (q, k, v, o_ref, lse_ref, time.perf_counter() - t0)
     return _REF[key]
 
 
@@ -66,7 +68,7 @@ def _run_split(q, k, v, causal, scale):
 def test_full_size_every_element(name, mode, path, monkeypatch):
     w = WORKLOADS[name]
     causal = mode == "causal"
-    q, k, v, o_ref, lse_ref = _reference(name, mode)
+    q, k, v, o_ref, lse_ref, oracle_s = _reference(name, mode)
     if path == "split":
         monkeypatch.setenv("FA2_SPLIT", "always")
         o, lse = _run_split(q, k, v, causal, w.scale)
@@ -75,7 +77,8 @@ def test_full_size_every_element(name, mode, path, monkeypatch):
     if causal:   # row 0 sees key 0 alone: O_0 = V_0 exactly
         assert torch.equal(o[:, :, 0], v[:, :, 0])
     rep = compare(o, lse, o_ref, lse_ref)
-    rep.update(workload=name, mode=mode, path=path)
+    rep.update(workload=name, mode=mode, path=path, oracle_seconds=round(oracle_s, 2),
+               oracle_threads=oracle.max_threads())
     print(json.dumps(rep))
     out = os.environ.get("FA2_PARITY_REPORT")
     if out:   # one JSON line per case, for the measured error table

@@ -56,7 +56,7 @@ def check(inputs, got, window, heads=None):
         assert err.max() <= REL_MAX * (max_ref if max_ref > 1e-6 else 1.0), (name, err.max(), max_ref)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("window", [0, 1, 63, 100, 200])
 def test_window_backward_every_element(D, window):
     """Ragged Lq < Lk: band edges inside and across the 64-row tiles of both kernels."""
