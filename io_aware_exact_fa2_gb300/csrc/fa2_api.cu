@@ -353,8 +353,8 @@ FA2_EXPORT fa2_status fa2_fwd_noalloc(const void *q, const void *k, const void *
         scratch = fa2::noalloc_scratch_ptr(dev);
         if (!scratch)
             return FA2_ERR_CUDA;
-        // the arrival counters (one int per CTA and Q tile, at most 4 Q tiles) start at zero
-        const size_t zero_bytes = fa2::align256(static_cast<size_t>(sms) * 4 * sizeof(int));
+        // the arrival counters (one int per CTA and Q tile, at most 2 Q tiles) start at zero
+        const size_t zero_bytes = fa2::align256(static_cast<size_t>(sms) * 2 * sizeof(int));
         if (cudaMemsetAsync(scratch, 0, zero_bytes < need ? zero_bytes : need, static_cast<cudaStream_t>(stream)) !=
             cudaSuccess) {
             (void)cudaGetLastError();

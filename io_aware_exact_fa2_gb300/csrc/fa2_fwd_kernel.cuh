@@ -206,23 +206,14 @@ struct FwdCfg {
     static constexpr int NUM_SOFTMAX_WARPS = 4 * CS * NQ;
     static constexpr int WARP_PRODUCER = NUM_SOFTMAX_WARPS;
     static constexpr int WARP_MMA = NUM_SOFTMAX_WARPS + 1;
-    // With two or four softmax warpgroups the control warpgroup drops to REG_CTRL
-    // registers and the softmax warpgroups rise to REG_SOFTMAX, within what the launch
-    // gives the block (LAUNCH_REGS per thread, the most 65536 registers allow):
-    //   two:  384 threads * 168 = 64512 = 2*128*200 + 128*104
-    //   four: 640 threads *  96 = 61440 = 4*128*104 + 128*64
-    static constexpr bool REG_SPLIT = (NUM_SOFTMAX_WARPS == 8 || NUM_SOFTMAX_WARPS == 16);
-#ifndef FA2_REG16_SOFTMAX
-#define FA2_REG16_SOFTMAX 104
-#endif
-#ifndef FA2_REG16_CTRL
-#define FA2_REG16_CTRL 64
-#endif
-    static constexpr int REG_SOFTMAX = NUM_SOFTMAX_WARPS == 16 ? FA2_REG16_SOFTMAX : 200;
-    static constexpr int REG_CTRL = NUM_SOFTMAX_WARPS == 16 ? FA2_REG16_CTRL : 104;
+    // With two softmax warpgroups the launch leaves 168 registers per thread; the
+    // control warpgroup drops to REG_CTRL and the softmax warpgroups rise to
+    // REG_SOFTMAX.  Budget: 2*128*200 + 128*104 = 64512 = 384 threads * 168.
+    static constexpr bool REG_SPLIT = (NUM_SOFTMAX_WARPS == 8);
+    static constexpr int REG_SOFTMAX = 200;
+    static constexpr int REG_CTRL = 104;
     static constexpr int NUM_THREADS = 32 * (NUM_SOFTMAX_WARPS + (REG_SPLIT ? 4 : 2));
-    static constexpr int LAUNCH_REGS = (65536 / NUM_THREADS) / 8 * 8 > 255 ? 255 : (65536 / NUM_THREADS) / 8 * 8;
-    static_assert(!REG_SPLIT || NUM_SOFTMAX_WARPS * 32 * REG_SOFTMAX + 128 * REG_CTRL <= NUM_THREADS * LAUNCH_REGS,
+    static_assert(!REG_SPLIT || 2 * 128 * REG_SOFTMAX + 128 * REG_CTRL <= NUM_THREADS * 168,
                   "register split exceeds the launch allocation");
 
     static constexpr uint32_t IDESC_S =
@@ -232,8 +223,7 @@ struct FwdCfg {
 
     static_assert(D % 64 == 0 && D >= 64 && D <= 256, "D must be 64, 128 or 256");
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 64 in [64, 256]");
-    static_assert(NQ == 1 || NQ == 2 || NQ == 4, "one, two or four Q tiles per work unit");
-    static_assert(NQ <= 2 || CS == 1, "four Q tiles take one softmax warp per row");
+    static_assert(NQ == 1 || NQ == 2, "one or two Q tiles per work unit");
     static_assert(CS == 1 || CS == 2, "one or two warps per row");
     static_assert(NS == 1 || NS == 2, "one or two S buffers per Q tile");
     static_assert(NCOL % 32 == 0 && OCOL % 32 == 0, "per-thread column slices are whole 32-column loads");
