@@ -15,13 +15,14 @@ namespace fa2 {
 // work finishes.
 //
 // D = 256: two CTAs per resident tile, each accumulating 128 of the 256 gradient
-// columns (both compute the step's full score products), and a one-stage ring: the
-// resident tiles (2 x 64 KB) and one stage of streamed tiles (2 x 32 KB) fill shared
-// memory; the dQ kernel's score products read Q and dO from shared memory.
+// columns (both compute the step's full score products).  The resident tiles take
+// 2 x 64 KB of shared memory, so the streamed tiles are 32 rows (16 KB each) through a
+// 3-stage ring, with one elementwise warp per lane quarter; the dQ kernel's score
+// products read Q and dO from shared memory.
 template <int D>
-using BwdKV = BwdCfg<D, 128, 64, (D == 256 ? 1 : 4), 8, (D == 256 ? 128 : D)>;
+using BwdKV = BwdCfg<D, 128, (D == 256 ? 32 : 64), (D == 256 ? 3 : 4), (D == 256 ? 4 : 8), (D == 256 ? 128 : D)>;
 template <int D>
-using BwdQ = BwdCfg<D, 128, 64, (D == 256 ? 1 : 4), 8, (D == 256 ? 128 : D)>;
+using BwdQ = BwdCfg<D, 128, (D == 256 ? 32 : 64), (D == 256 ? 3 : 4), (D == 256 ? 4 : 8), (D == 256 ? 128 : D)>;
 static_assert(BWD_STAT_TILE_ROWS == BWD_STAT_ROWS, "workspace sizing and kernels agree on the statistics tiles");
 
 template <class K>

@@ -15,9 +15,10 @@
 //
 // GB300 mapping, per kernel:
 //   * TMA (128B swizzle) moves the resident tiles once and the streamed tiles
-//     through a ring; one warp issues tcgen05.mma (elected lane); eight warps
-//     do the elementwise work, two per 32-lane TMEM quarter (one TMEM lane = one
-//     row), each with half of a step's columns.
+//     through a ring; one warp issues tcgen05.mma (elected lane); the
+//     elementwise warps own 32-lane TMEM quarters (one TMEM lane = one row), two
+//     per quarter with half of a step's 64 columns each, or (D = 256, 32-row
+//     steps) one per quarter.
 //   * The two score-like products of a step (S and dP, or their transposes)
 //     go into one of two TMEM buffer pairs, so the next step's pair is computed
 //     while the elementwise warps work on this one.  P and dS are written back
@@ -25,7 +26,7 @@
 //     streamed tiles serve as the MMA's B operand both K-major (for S, dP) and
 //     MN-major (for dV, dK, dQ) without a transpose pass.
 //   * The Delta kernel also writes each query row's -lse * log2 e beside -Delta,
-//     in 64-row tiles, so a streamed query tile's statistics ride one bulk copy
+//     in 64-row tiles, so a streamed query tile's statistics ride bulk copies
 //     on the same ring barrier as its Q and dO tiles (no global loads in the
 //     producer's loop).
 //   * Every wait is bounded (a device error word records which one ran out).
@@ -286,8 +287,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                       const BwdParams p)
 {
     using namespace ptx;
-    static_assert(C::STR == BWD_STAT_ROWS, "one statistics tile per streamed query tile");
-    static_assert(C::EW == 8 && C::STR == 64, "two elementwise warps of 32 query columns per lane quarter");
+    static_assert(BWD_STAT_ROWS % C::STR == 0, "a streamed query tile lies in one statistics tile");
+    static_assert((C::EW == 8 && C::STR == 64) || (C::EW == 4 && C::STR == 32),
+                  "32 query columns per elementwise warp: two warps per lane quarter at 64, one at 32");
     constexpr int TM_DV = 0, TM_DK = C::DH, TM_ST = 2 * C::DH, TM_DPT = 2 * C::DH + 2 * C::STR;
     constexpr int TMEM_COLS = 512;
     static_assert(TM_DPT + 2 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
@@ -362,9 +364,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                                  bar(C::BAR_RES_FULL));
                 }
             }
-            // this head's statistics tiles from query tile qt0 on (-lse2 and -Delta,
-            // 2 * STR floats per tile, one bulk copy per step)
-            const float *stat_src = p.stats + (static_cast<size_t>(bh) * p.n_stat_tiles + qt0) * 2 * C::STR;
+            // this head's statistics tiles (-lse2 and -Delta of BWD_STAT_ROWS rows each): a
+            // step's STR rows of both, one bulk copy each (one copy when STR fills a tile)
+            const float *stat_head = p.stats + static_cast<size_t>(bh) * p.n_stat_tiles * 2 * BWD_STAT_ROWS;
             for (int s = 0; s < n_steps && ok; ++s) {
                 const int st = s % C::RING;
                 if (s >= C::RING)
@@ -376,8 +378,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const int q0 = (qt0 + s) * C::STR;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar(C::BAR_STR_FULL + st), 2 * C::STR_TILE + C::STAT_BYTES);
-                    bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES, stat_src + s * 2 * C::STR, C::STAT_BYTES,
-                              bar(C::BAR_STR_FULL + st));
+                    const float *stat_src = stat_head + (q0 / BWD_STAT_ROWS) * 2 * BWD_STAT_ROWS + q0 % BWD_STAT_ROWS;
+                    if constexpr (C::STR < BWD_STAT_ROWS) {
+                        bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES, stat_src, C::STR * 4,
+                                  bar(C::BAR_STR_FULL + st));
+                        bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES + C::STR * 4, stat_src + BWD_STAT_ROWS,
+                                  C::STR * 4, bar(C::BAR_STR_FULL + st));
+                    } else {
+                        bulk_load(sbase + C::OFF_STAT + st * C::STAT_BYTES, stat_src, C::STAT_BYTES,
+                                  bar(C::BAR_STR_FULL + st));
+                    }
 #pragma unroll
                     for (int c = 0; c < C::DB; ++c) {
                         bwd_tma_load(sbase + C::OFF_STR0 + st * C::STR_TILE + c * C::STR_BLOCK, &tm_q, q3,
@@ -474,7 +484,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     } else {
         // ------------------------------------------------ elementwise warps
         // Two warps per 32-lane TMEM quarter: `half` 0 takes query columns 0..31 of
-        // every step (and stores dV), `half` 1 columns 32..63 (and stores dK).
+        // every step (and stores dV), `half` 1 columns 32..63 (and stores dK).  With
+        // one warp per quarter (32-column steps) that warp does both.
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;         // key row within the tile (TMEM lane)
         const int kj = k0 + row;                     // key index
@@ -556,20 +567,28 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (lane == 0)
                 mbar_arrive(bar(C::BAR_GRAD_READY + b));
         }
-        // epilogue: dV (half 0) or scale * dK (half 1) rows; zeros when no query sees
-        // these keys
+        // epilogue: dV (half 0) or scale * dK (half 1) rows, both with one warp per
+        // quarter; zeros when no query sees these keys
         const bool valid = kj < p.Lk;
         const long long ob = hb, oh = hh, orow = valid ? kj : 0;
-        uint16_t *out_row = (half ? p.dk + ob * p.dk_sb + oh * p.dk_sh + orow * p.dk_sl
-                                  : p.dv + ob * p.dv_sb + oh * p.dv_sh + orow * p.dv_sl) + dh * C::DH;
+        uint16_t *dv_row = p.dv + ob * p.dv_sb + oh * p.dv_sh + orow * p.dv_sl + dh * C::DH;
+        uint16_t *dk_row = p.dk + ob * p.dk_sb + oh * p.dk_sh + orow * p.dk_sl + dh * C::DH;
+        const bool do_v = C::EW == 4 || half == 0, do_k = C::EW == 4 || half == 1;
         if (n_steps == 0) {
             if (valid) {
-                for (int d = 0; d < C::DH; d += 8)
-                    *reinterpret_cast<uint4 *>(out_row + d) = make_uint4(0, 0, 0, 0);
+                for (int d = 0; d < C::DH; d += 8) {
+                    if (do_v)
+                        *reinterpret_cast<uint4 *>(dv_row + d) = make_uint4(0, 0, 0, 0);
+                    if (do_k)
+                        *reinterpret_cast<uint4 *>(dk_row + d) = make_uint4(0, 0, 0, 0);
+                }
             }
         } else if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 2, p.wait_limit_ns)) {
             tc_fence_after();
-            store_acc_row<C::DH>(tmem + lane_base + (half ? TM_DK : TM_DV), half ? p.scale : 1.f, out_row, valid);
+            if (do_v)
+                store_acc_row<C::DH>(tmem + lane_base + TM_DV, 1.f, dv_row, valid);
+            if (do_k)
+                store_acc_row<C::DH>(tmem + lane_base + TM_DK, p.scale, dk_row, valid);
         }
     }
 
@@ -593,7 +612,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                      const BwdParams p)
 {
     using namespace ptx;
-    static_assert(C::EW == 8 && C::STR == 64, "two elementwise warps of 32 key columns per lane quarter");
+    static_assert((C::EW == 8 && C::STR == 64) || (C::EW == 4 && C::STR == 32),
+                  "32 key columns per elementwise warp: two warps per lane quarter at 64, one at 32");
+    static_assert(!C::RES_IN_TMEM || C::EW == 8, "Q and dO are copied into TMEM by the two warps of a quarter");
     // Q and dO are also copied into TMEM (TM_QA, TM_DOA) so that S = Q K^T and
     // dP = dO V^T read their A operand from TMEM instead of loading it from shared
     // memory for every instruction
@@ -787,7 +808,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     } else {
         // ------------------------------------------------ elementwise warps
         // Two warps per 32-lane TMEM quarter: `half` 0 takes key columns 0..31 of
-        // every step, `half` 1 columns 32..63; each stores half of dQ's columns.
+        // every step, `half` 1 columns 32..63; each stores half of dQ's columns.  With
+        // one warp per quarter (32-column steps) it takes them all.
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;         // query row within the tile (TMEM lane)
         const int qi = q0 + row;
@@ -880,15 +902,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if (lane == 0)
                 mbar_arrive(bar(C::BAR_GRAD_READY + b));
         }
-        // epilogue: scale * dQ, columns dh * DH + [half * DH/2, (half + 1) * DH/2) of this row
+        // epilogue: scale * dQ, columns dh * DH + [half * W, (half + 1) * W) of this row, W the
+        // columns per warp of a lane quarter (DH / 2 with two warps, DH with one)
+        constexpr int W = C::DH / (C::EW / 4);
         if (ok && warp_wait_all(bar(C::BAR_DONE), 0, p.err, ERR_BWD_ELEM | 4, p.wait_limit_ns)) {
             tc_fence_after();
-            store_acc_row<C::DH / 2>(tmem + lane_base + TM_DQ + half * (C::DH / 2), p.scale,
-                                     p.dq + static_cast<long long>(hb) * p.dq_sb +
-                                         static_cast<long long>(hh) * p.dq_sh +
-                                         static_cast<long long>(live ? qi : 0) * p.dq_sl + dh * C::DH +
-                                         half * (C::DH / 2),
-                                     live);
+            store_acc_row<W>(tmem + lane_base + TM_DQ + half * W, p.scale,
+                             p.dq + static_cast<long long>(hb) * p.dq_sb + static_cast<long long>(hh) * p.dq_sh +
+                                 static_cast<long long>(live ? qi : 0) * p.dq_sl + dh * C::DH + half * W,
+                             live);
         }
     }
 
