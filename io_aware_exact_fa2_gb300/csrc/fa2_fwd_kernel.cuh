@@ -155,11 +155,13 @@ struct FwdCfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * KV_TILE;
-    // O staging of the epilogue: each softmax warp's 32 rows x OBW columns of bf16
-    // (64 columns, 128B-swizzled; 32 columns, 64B-swizzled, when a warp owns only 32
-    // columns of a row), the shared-memory side of one TMA store box
-    static constexpr int OBW = (D / CS) >= 64 ? 64 : 32;
-    static constexpr int O_STAGE = 32 * OBW * 2;
+    // O staging of the epilogue: each softmax warp has two halves, each the
+    // shared-memory side of one TMA store box of its 32 rows x OBW = 32 columns of bf16
+    // (64-byte rows, 64B-swizzled); consecutive boxes alternate halves, so a warp
+    // fills one while the store of the other is still reading it
+    static constexpr int OBW = 32;
+    static constexpr int O_HALF = 32 * OBW * 2;
+    static constexpr int O_STAGE = 2 * O_HALF;
     static constexpr int OFF_OST = OFF_V + KS * KV_TILE;                // [softmax warps] (1024-aligned)
     static constexpr int OFF_XMAX = OFF_OST + 4 * CS * NQ * O_STAGE;   // f32 [NQ][2][CS][128] (CS > 1)
     static constexpr int OFF_XL = OFF_XMAX + (CS > 1 ? NQ * 2 * CS * 128 * 4 : 0);  // f32x2 [NQ][CS][128] (CS > 1)
@@ -231,8 +233,8 @@ struct FwdCfg {
     static_assert(!QT || NQ == 1, "Q in TMEM needs one Q tile per unit");
     static_assert(!QT || (D / CS) % 64 == 0, "Q copy works on whole 64-column swizzle blocks");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget exceeded");
-    static_assert(OFF_OST % 1024 == 0 && O_STAGE % 1024 == 0,
-                  "a swizzled TMA box needs an aligned shared-memory side (1024 bytes covers both swizzles)");
+    static_assert(OFF_OST % 1024 == 0 && O_HALF % 512 == 0,
+                  "a 64B-swizzled TMA box needs a 512-byte aligned shared-memory side");
     static_assert((D / CS) % OBW == 0, "a warp's O columns are whole store boxes");
     static_assert(!P2 || CS == 1, "two-term P keeps a row's residuals beside its own weights (one warp per row)");
     static_assert(!F8 || (!QT && !P2 && CS == 1 && D % 128 == 0), "e4m3 path: Q in shared memory, one-term P, "
@@ -682,6 +684,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t o_addr = tmem + lane_base + C::TM_O + t * C::D + h * C::OCOL;
         const uint32_t o_stage = sbase + C::OFF_OST + warp * C::O_STAGE;   // this warp's O staging
+        uint32_t o_boxes = 0;   // O boxes this warp has staged (their half alternates)
         const uint32_t xmax = sbase + C::OFF_XMAX + t * (2 * C::CS * 128 * 4);
         const uint32_t xl = sbase + C::OFF_XL + t * (C::CS * 128 * 8);
         // one arrival per warp: every lane's prior writes (shared memory, and TMEM
@@ -1032,33 +1035,42 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const bool live = grow < p.Lq;
             const size_t out_row = static_cast<size_t>(bh) * p.Lq + (live ? grow : 0);
             const bool whole = sg.c_first == sg.c_last;
-            // O leaves through the warp's staging buffer, one OBW-column block at a time:
-            // o_block_begin waits until the previous TMA store has read the buffer,
-            // o_block_put writes 16 bf16 words (32 columns) of this thread's row, and
-            // o_block_store writes the warp's 32 rows x OBW columns with one TMA store
-            // (whole lines of its rows; rows past Lq lie outside the tensor map and are
-            // not written).
-            auto o_block_begin = [&]() {
+            // O leaves through the warp's staging halves, one 32-column box at a time:
+            // o_block_begin waits until the store that last read the next half is done
+            // with it (at most one store, the other half's, may still be reading) and
+            // returns that half, o_block_put writes 16 bf16 words (32 columns) of this
+            // thread's row into it, and o_block_store writes the warp's 32 rows x 32
+            // columns with one TMA store (whole 64-byte pieces of its rows; rows past Lq
+            // lie outside the tensor map and are not written).
+            auto o_block_begin = [&]() -> uint32_t {
                 if (lane == 0)
-                    bulk_wait_group_read0();
+                    bulk_wait_group_read1();
                 __syncwarp();
+                return o_stage + (o_boxes & 1) * C::O_HALF;
             };
-            // (16-byte chunk k of row r sits at k ^ (r % 8) in 128-byte rows under the 128B
-            // swizzle, at k ^ ((r / 2) % 4) in 64-byte rows under the 64B swizzle)
-            auto o_block_put = [&](int hf, const uint32_t (&w)[16]) {
-                const uint32_t rowp = o_stage + lane * (C::OBW * 2);
-                const int sw = C::OBW == 64 ? (lane & 7) : ((lane >> 1) & 3);
+            // (16-byte chunk k of row r sits at k ^ ((r / 2) % 4) in 64-byte rows under the
+            // 64B swizzle)
+            auto o_block_put = [&](uint32_t buf, const uint32_t (&w)[16]) {
+                const uint32_t rowp = buf + lane * (C::OBW * 2);
+                const int sw = (lane >> 1) & 3;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    st_shared_v4(rowp + (((4 * hf + c) ^ sw) * 16), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    st_shared_v4(rowp + ((c ^ sw) * 16), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
             };
-            auto o_block_store = [&](int bq) {
+            auto o_block_store = [&](uint32_t buf, int bq) {
                 fence_proxy_async_shared();
                 __syncwarp();
-                if (lane == 0 && q0_t + quarter * 32 < p.Lq) {
-                    tma_store_4d(&tm_o, o_stage, h * C::OCOL + C::OBW * bq, q0_t + quarter * 32, bh % p.H, bh / p.H);
-                    bulk_commit_group();
+                if (lane == 0) {
+                    if (q0_t + quarter * 32 < p.Lq) {
+                        tma_store_4d(&tm_o, buf, h * C::OCOL + C::OBW * bq, q0_t + quarter * 32, bh % p.H, bh / p.H);
+                        bulk_commit_group();
+                    } else {
+                        // no store for rows past Lq: with no group committed for this box,
+                        // the next begin's one-pending allowance must not cover its half
+                        bulk_wait_group_read0();
+                    }
                 }
+                ++o_boxes;
             };
             // this part's workspace rows (cut units only): LSE pairs by row, O as float4
             // column groups of 128 rows each
@@ -1104,10 +1116,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const float4 *part4 = reinterpret_cast<const float4 *>(p.part_o);
 #pragma unroll 1
                 for (int bq = 0; bq < C::OCOL / C::OBW; ++bq) {
-                  o_block_begin();
-#pragma unroll
-                  for (int hf = 0; hf < C::OBW / 32; ++hf) {
-                    const int cc = (C::OBW / 32) * bq + hf;
+                  const int cc = bq;   // one 32-column TMEM chunk per box
+                  {
                     const size_t col4 = static_cast<size_t>((h * C::OCOL + 32 * cc) / 4) * 128 + row;
                     // this CTA's own part, read out of TMEM when its turn in the sum comes
                     auto load_own = [&](float4 *dst) {
@@ -1164,9 +1174,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         w[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
-                    o_block_put(hf, w);
+                    const uint32_t buf = o_block_begin();
+                    o_block_put(buf, w);
+                    o_block_store(buf, bq);
                   }
-                  o_block_store(bq);
                 }
                 if (h == 0 && live)
                     p.lse[out_row] = (mx + lg2_approx(xsum)) * LN2;
@@ -1193,14 +1204,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 if (h == 0 && row == 0)
                     atomicExch(counter, 0);   // leave the workspace ready for the next call
             } else {
-                float4 *ptile = whole ? nullptr : reinterpret_cast<float4 *>(p.part_o) + part_tile * (C::D / 4) * 128;
+                if (whole) {
+                    // one 32-column chunk at a time (loading more of them at once measured
+                    // slower: the registers they hold cost the step loop), each staged in
+                    // the half that the store before last has finished reading
 #pragma unroll 1
-                for (int bq = 0; bq < C::OCOL / C::OBW; ++bq) {
-                    if (whole)
-                        o_block_begin();
-#pragma unroll
-                    for (int hf = 0; hf < C::OBW / 32; ++hf) {
-                        const int cc = (C::OBW / 32) * bq + hf;
+                    for (int cc = 0; cc < C::OCOL / 32; ++cc) {
                         uint32_t r[32];
                         tmem_ld32(o_addr + 32 * cc, r);
                         tmem_ld_wait(r);
@@ -1209,23 +1218,32 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                             tc_fence_before();
                             warp_arrive(bar(C::BAR_O_FREE + t));
                         }
-                        if (whole) {
-                            uint32_t w[16];
+                        uint32_t w[16];
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-                            o_block_put(hf, w);
-                        } else {
-                            const int g0 = (h * C::OCOL + 32 * cc) / 4;   // first float4 column group
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                ptile[(g0 + q) * 128 + row] = make_float4(
-                                    __uint_as_float(r[4 * q]) * inv_l, __uint_as_float(r[4 * q + 1]) * inv_l,
-                                    __uint_as_float(r[4 * q + 2]) * inv_l, __uint_as_float(r[4 * q + 3]) * inv_l);
-                        }
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+                        const uint32_t buf = o_block_begin();
+                        o_block_put(buf, w);
+                        o_block_store(buf, cc);
                     }
-                    if (whole)
-                        o_block_store(bq);
+                } else {
+                    float4 *ptile = reinterpret_cast<float4 *>(p.part_o) + part_tile * (C::D / 4) * 128;
+#pragma unroll 1
+                    for (int cc = 0; cc < C::OCOL / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + 32 * cc, r);
+                        tmem_ld_wait(r);
+                        if (cc == C::OCOL / 32 - 1) {
+                            tc_fence_before();
+                            warp_arrive(bar(C::BAR_O_FREE + t));
+                        }
+                        const int g0 = (h * C::OCOL + 32 * cc) / 4;   // first float4 column group
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            ptile[(g0 + q) * 128 + row] = make_float4(
+                                __uint_as_float(r[4 * q]) * inv_l, __uint_as_float(r[4 * q + 1]) * inv_l,
+                                __uint_as_float(r[4 * q + 2]) * inv_l, __uint_as_float(r[4 * q + 3]) * inv_l);
+                    }
                 }
                 if (whole) {
                     if (h == 0 && live)

@@ -204,6 +204,9 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 // Wait until this thread's bulk stores have finished reading their shared-memory source.
 __device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// ... all but the most recent bulk group.
+__device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // Wait until this thread's bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

@@ -121,7 +121,7 @@ def test_deterministic(D):
         assert torch.equal(x, y)
 
 
-def delta_term(q, k, v, do, o_stored, scale, heads):
+def delta_term(q, k, v, do, o_stored, scale, heads, ref=None, o_exact=None):
     """Relative rms, per gradient, of the error that Delta = rowsum(dO * O) takes from the
     STORED (bf16) O ("Chapter 08: Flash Attention -- blocked attention", section 6.2
     defines Delta from the forward's output): dDelta_i = sum_d dO_id (O~_id - O_id), and
@@ -131,8 +131,10 @@ def delta_term(q, k, v, do, o_stored, scale, heads):
     import oracle as orc
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
-    dq, dk, _, _ = orc.gradients(q, k, v, do, False, scale, heads=heads)   # only their rms is used
-    o_exact, _ = orc.attention(q, k, v, False, scale)
+    # the oracle's gradients of these heads (only their rms is used) and its exact O, unless given
+    dq, dk = ref[:2] if ref is not None else orc.gradients(q, k, v, do, False, scale, heads=heads)[:2]
+    if o_exact is None:
+        o_exact, _ = orc.attention(q, k, v, False, scale)
     out = ("dq", "dk")
     Q, K, DO = (t.double().numpy().reshape(B * H, -1, D)[heads] for t in (q, k, do))
     OE = o_exact.reshape(B * H, Lq, D)[heads]
