@@ -9,7 +9,8 @@
 namespace fa2 {
 
 // dK/dV: 128 keys resident, query tiles of 64 streamed through a 4-stage ring
-// (dV, dK and two 64-column score pairs fill TMEM; K and V stay in shared memory);
+// (dV, dK and two 64-column score pairs fill TMEM at D = 128, where K and V stay in
+// shared memory; at D = 64 K is also copied into TMEM as the score products' A operand);
 // dQ: 128 queries resident, key tiles of 64 through a 4-stage ring.  Two score
 // buffer pairs let one step's MMAs run while the previous step's elementwise
 // work finishes.
@@ -17,8 +18,9 @@ namespace fa2 {
 // D = 256: two CTAs per resident tile, each accumulating 128 of the 256 gradient
 // columns (both compute the step's full score products).  The resident tiles take
 // 2 x 64 KB of shared memory, so the streamed tiles are 32 rows (16 KB each) through a
-// 3-stage ring, with one elementwise warp per lane quarter; the dQ kernel's score
-// products read Q and dO from shared memory.
+// 3-stage ring, with one elementwise warp per lane quarter.  The 32-column score
+// buffers leave TMEM room for Q and dO (dQ kernel) and for K (dK/dV kernel) as the A
+// operands of the score products.
 template <int D>
 using BwdKV = BwdCfg<D, 128, (D == 256 ? 32 : 64), (D == 256 ? 3 : 4), (D == 256 ? 4 : 8), (D == 256 ? 128 : D)>;
 template <int D>

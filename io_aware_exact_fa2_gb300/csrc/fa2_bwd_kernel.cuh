@@ -174,9 +174,18 @@ struct BwdCfg {
     // score pairs issued ahead of the gradient MMAs: two buffer pairs, but never more
     // than the ring holds (a pair waits for its stage's tiles)
     static constexpr int LA = RING >= 2 ? 2 : 1;
-    // the dQ kernel keeps Q and dO as TMEM A operands where TMEM has room (D <= 128);
-    // otherwise its score products read them from shared memory
-    static constexpr bool RES_IN_TMEM = D <= 128;
+    // the dQ kernel keeps Q and dO as TMEM A operands where TMEM has room beside dQ and
+    // the two score-buffer pairs; otherwise its score products read them from shared
+    // memory
+    static constexpr bool RES_IN_TMEM = DH + 4 * STR + D <= 512;
+    // likewise the dK/dV kernel keeps K as the TMEM A operand of S^T = K Q^T where it fits
+    // beside dV, dK and the score buffers (D = 64 and 256; V stays in shared memory).  A
+    // score MMA with its A operand in shared memory re-reads all of A for each
+    // instruction, which bounds the narrow (N = STR) score products.
+#ifndef FA2_BWD_K_IN_TMEM
+#define FA2_BWD_K_IN_TMEM 1
+#endif
+    static constexpr bool K_IN_TMEM = FA2_BWD_K_IN_TMEM && 2 * DH + 4 * STR + D / 2 <= 512;
     static constexpr int DB = D / 64;    // 64-column (128-byte) swizzle blocks
     static constexpr int RES_BLOCK = RES * 128;
     static constexpr int RES_TILE = DB * RES_BLOCK;
@@ -291,8 +300,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     static_assert((C::EW == 8 && C::STR == 64) || (C::EW == 4 && C::STR == 32),
                   "32 query columns per elementwise warp: two warps per lane quarter at 64, one at 32");
     constexpr int TM_DV = 0, TM_DK = C::DH, TM_ST = 2 * C::DH, TM_DPT = 2 * C::DH + 2 * C::STR;
+    constexpr int TM_KA = TM_DPT + 2 * C::STR;   // K as packed bf16 pairs (K_IN_TMEM only)
     constexpr int TMEM_COLS = 512;
-    static_assert(TM_DPT + 2 * C::STR <= TMEM_COLS, "TMEM budget exceeded");
+    static_assert(TM_KA + (C::K_IN_TMEM ? C::D / 2 : 0) <= TMEM_COLS, "TMEM budget exceeded");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -426,6 +436,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const uint64_t desc_k = sdesc_sw128(sbase + C::OFF_RES0, 16, 1024);
                 const uint64_t desc_v = sdesc_sw128(sbase + C::OFF_RES1, 16, 1024);
                 ok = lone_wait(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_MMA | 1, p.wait_limit_ns);
+                if (C::K_IN_TMEM && ok)   // K copied into TMEM by the elementwise warps
+                    ok = lone_wait(bar(C::BAR_RES_TMEM), 0, p.err, ERR_BWD_MMA | 9, p.wait_limit_ns);
                 tc_fence_after();
                 const auto stage_off = [](int st) { return static_cast<uint64_t>((st * C::STR_TILE) >> 4); };
                 // S^T(b) = K Q^T and dP^T(b) = V dO^T for step s
@@ -439,8 +451,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                     for (int kk = 0; kk < C::D / 16; ++kk) {
                         const uint64_t ko = static_cast<uint64_t>(((kk >> 2) * C::RES_BLOCK + (kk & 3) * 32) >> 4);
                         const uint64_t to = static_cast<uint64_t>(((kk >> 2) * C::STR_BLOCK + (kk & 3) * 32) >> 4);
-                        mma_ss(tmem + TM_ST + b * C::STR, desc_k + ko, desc_q + stage_off(st) + to, C::IDESC_PAIR,
-                               kk > 0 ? 1u : 0u);
+                        if constexpr (C::K_IN_TMEM)
+                            mma_ts(tmem + TM_ST + b * C::STR, tmem + TM_KA + kk * 8, desc_q + stage_off(st) + to,
+                                   C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                        else
+                            mma_ss(tmem + TM_ST + b * C::STR, desc_k + ko, desc_q + stage_off(st) + to,
+                                   C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                         mma_ss(tmem + TM_DPT + b * C::STR, desc_v + ko, desc_do + stage_off(st) + to, C::IDESC_PAIR,
                                kk > 0 ? 1u : 0u);
                     }
@@ -493,6 +509,20 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const int c0 = 32 * half;                    // this warp's first query column of a step
         const float c2 = p.scale_log2;
         bool ok = true;
+        if (C::K_IN_TMEM && n_steps > 0) {
+            // this row of K into TMEM (the first warp of each quarter), as the A operand of
+            // S^T = K Q^T
+            ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 7, p.wait_limit_ns);
+            if (ok) {
+                if (half == 0)
+                    copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_KA);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar(C::BAR_RES_TMEM));
+            }
+        }
         for (int s = 0; s < n_steps && ok; ++s) {
             const int st = s % C::RING, b = s & 1;
             ok = warp_wait_all(bar(C::BAR_SCORE_FULL + b), (s >> 1) & 1, p.err, ERR_BWD_ELEM | 1, p.wait_limit_ns);
@@ -614,7 +644,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     using namespace ptx;
     static_assert((C::EW == 8 && C::STR == 64) || (C::EW == 4 && C::STR == 32),
                   "32 key columns per elementwise warp: two warps per lane quarter at 64, one at 32");
-    static_assert(!C::RES_IN_TMEM || C::EW == 8, "Q and dO are copied into TMEM by the two warps of a quarter");
     // Q and dO are also copied into TMEM (TM_QA, TM_DOA) so that S = Q K^T and
     // dP = dO V^T read their A operand from TMEM instead of loading it from shared
     // memory for every instruction
@@ -828,9 +857,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         // this row of Q (half 0) or of dO (half 1) into TMEM, as a score MMA's A operand
         bool ok = !C::RES_IN_TMEM || warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 6, p.wait_limit_ns);
         if (ok && C::RES_IN_TMEM) {
+            // two warps per quarter: one copies Q, the other dO; one warp per quarter: both
             if (half == 0)
                 copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_QA);
-            else
+            if (half == 1 || C::EW == 4)
                 copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES1, row, tmem + lane_base + TM_DOA);
             tmem_st_wait();
             tc_fence_before();
