@@ -10,7 +10,8 @@ namespace fa2 {
 
 // dK/dV: 128 keys resident, query tiles of 64 streamed through a 4-stage ring
 // (dV, dK and two 64-column score pairs fill TMEM at D = 128, where K and V stay in
-// shared memory; at D = 64 K is also copied into TMEM as the score products' A operand);
+// shared memory; at D = 64 K and V are also copied into TMEM as the score products' A
+// operands);
 // dQ: 128 queries resident, key tiles of 64 through a 4-stage ring.  Two score
 // buffer pairs let one step's MMAs run while the previous step's elementwise
 // work finishes.

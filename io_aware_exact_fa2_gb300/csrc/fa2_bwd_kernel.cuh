@@ -186,6 +186,8 @@ struct BwdCfg {
 #define FA2_BWD_K_IN_TMEM 1
 #endif
     static constexpr bool K_IN_TMEM = FA2_BWD_K_IN_TMEM && 2 * DH + 4 * STR + D / 2 <= 512;
+    // and V as the A operand of dP^T = V dO^T, where both fit (D = 64)
+    static constexpr bool V_IN_TMEM = K_IN_TMEM && 2 * DH + 4 * STR + D <= 512;
     static constexpr int DB = D / 64;    // 64-column (128-byte) swizzle blocks
     static constexpr int RES_BLOCK = RES * 128;
     static constexpr int RES_TILE = DB * RES_BLOCK;
@@ -301,8 +303,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                   "32 query columns per elementwise warp: two warps per lane quarter at 64, one at 32");
     constexpr int TM_DV = 0, TM_DK = C::DH, TM_ST = 2 * C::DH, TM_DPT = 2 * C::DH + 2 * C::STR;
     constexpr int TM_KA = TM_DPT + 2 * C::STR;   // K as packed bf16 pairs (K_IN_TMEM only)
+    constexpr int TM_VA = TM_KA + C::D / 2;      // V likewise (V_IN_TMEM only)
     constexpr int TMEM_COLS = 512;
-    static_assert(TM_KA + (C::K_IN_TMEM ? C::D / 2 : 0) <= TMEM_COLS, "TMEM budget exceeded");
+    static_assert(TM_KA + (C::K_IN_TMEM ? C::D / 2 : 0) + (C::V_IN_TMEM ? C::D / 2 : 0) <= TMEM_COLS,
+                  "TMEM budget exceeded");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -457,8 +461,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                         else
                             mma_ss(tmem + TM_ST + b * C::STR, desc_k + ko, desc_q + stage_off(st) + to,
                                    C::IDESC_PAIR, kk > 0 ? 1u : 0u);
-                        mma_ss(tmem + TM_DPT + b * C::STR, desc_v + ko, desc_do + stage_off(st) + to, C::IDESC_PAIR,
-                               kk > 0 ? 1u : 0u);
+                        if constexpr (C::V_IN_TMEM)
+                            mma_ts(tmem + TM_DPT + b * C::STR, tmem + TM_VA + kk * 8, desc_do + stage_off(st) + to,
+                                   C::IDESC_PAIR, kk > 0 ? 1u : 0u);
+                        else
+                            mma_ss(tmem + TM_DPT + b * C::STR, desc_v + ko, desc_do + stage_off(st) + to,
+                                   C::IDESC_PAIR, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(bar(C::BAR_SCORE_FULL + b));
                     return true;
@@ -511,11 +519,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         bool ok = true;
         if (C::K_IN_TMEM && n_steps > 0) {
             // this row of K into TMEM (the first warp of each quarter), as the A operand of
-            // S^T = K Q^T
+            // S^T = K Q^T, and (V_IN_TMEM) of V (the second warp), for dP^T = V dO^T
             ok = warp_wait_all(bar(C::BAR_RES_FULL), 0, p.err, ERR_BWD_ELEM | 7, p.wait_limit_ns);
             if (ok) {
                 if (half == 0)
                     copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES0, row, tmem + lane_base + TM_KA);
+                if (C::V_IN_TMEM && (half == 1 || C::EW == 4))
+                    copy_row_to_tmem<C::DB, C::RES_BLOCK>(sbase + C::OFF_RES1, row, tmem + lane_base + TM_VA);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
