@@ -144,7 +144,7 @@ def _strided_bwd(q, k, v, do, o, lse, grads, causal, scale, window=None):
     return grads
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["noncausal", "causal"])
 def test_bwd_blhd_views_match_contiguous(D, causal):
     """Every tensor of the backward stored as [B, L, H, D] and viewed as [B, H, L, D]:
