@@ -55,14 +55,17 @@ def kernel_digest() -> str:
     """Hash of the sources that decide what the forward kernel does on the device: the
     kernel template, its PTX wrappers, the launch logic and the per-D instantiations (not
     the C ABI wrapper or the header), so that recorded profiler counters stay valid
-    across host-only changes."""
+    across host-only changes.  Whole-line comments and blank lines are left out, so a
+    change to them alone keeps the recorded counters."""
     h = hashlib.sha256()
     files = sorted(f for f in os.listdir(CSRC)
                    if f in ("fa2_fwd_kernel.cuh", "sm103_ptx.cuh", "fa2_launch.cuh", "fa2_split_ranges.h")
                    or (f.startswith("fa2_fwd_") and f.endswith(".cu")))
     for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+            code = [ln.rstrip() for ln in fh.read().split(b"\n")]
+        code = [ln for ln in code if ln.strip() and not ln.lstrip().startswith(b"//")]
+        h.update(f.encode() + b"\0" + b"\n".join(code))
     return h.hexdigest()[:16]
 
 

@@ -41,8 +41,9 @@
 //     is exact because l and LSE use the same max).
 //   * Epilogue: the softmax warps read O out of TMEM, release it to the MMA
 //     warp (the next unit's PV may then overwrite it), multiply by 1/l, stage
-//     bf16 blocks of 32 rows x 64 columns in shared memory and write each with
-//     one TMA store (whole 128-byte lines); the fp32 LSE goes straight out.
+//     bf16 boxes of 32 rows x 32 columns in two alternating halves of a per-warp
+//     shared-memory buffer and write each with one TMA store; the fp32 LSE goes
+//     straight out.
 //   * Every wait between warps is on an mbarrier with a time bound; a wait
 //     that runs out records a code in a device error word and the CTA winds
 //     down, so no input can hang the GPU.
