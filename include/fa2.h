@@ -259,7 +259,7 @@ fa2_status fa2_fwd_fp8(const void *q, const void *k, const void *v,
  * fa2_bwd_workspace_size -- bytes of device workspace fa2_bwd needs: two fp32
  * per query row (-lse * log2 e and -Delta), rows padded to a multiple of 64
  * per head.  Returns FA2_OK; FA2_ERR_INVALID_ARG for bad sizes;
- * FA2_ERR_UNSUPPORTED for D other than 64 or 128.
+ * FA2_ERR_UNSUPPORTED for D other than 64, 128 or 256.
  */
 fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, size_t *bytes);
 
@@ -280,7 +280,9 @@ fa2_status fa2_bwd_workspace_size(int B, int H, int Lq, int Lk, int D, size_t *b
  *   dq           device bf16 [B, H, Lq, D] output.
  *   dk, dv       device bf16 [B, H, Lk, D] outputs (zero rows for keys no
  *                query sees, e.g. causal keys beyond the last query).
- *   D            64 or 128 (FA2_ERR_UNSUPPORTED otherwise).
+ *   D            64, 128 or 256 (FA2_ERR_UNSUPPORTED otherwise).  At 256 two CTAs
+ *                share each resident tile, each accumulating half of the
+ *                gradient columns.
  *   workspace    device pointer, 16-byte aligned, at least
  *                fa2_bwd_workspace_size() bytes; overwritten (may be NULL
  *                when Lq == 0, where dk and dv are simply zeroed).
