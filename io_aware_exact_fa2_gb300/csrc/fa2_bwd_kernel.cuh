@@ -288,9 +288,11 @@ __device__ __forceinline__ void bwd_cta_tile(int idx, int n_tiles, const BwdPara
 
 // ============================================================== dK, dV kernel
 // CTA = one tile of RES = 128 keys of one (b, h); steps = query tiles of STR rows.
-// TMEM: dV (D cols), dK (D cols), two S^T buffers and two dP^T buffers (STR cols
+// TMEM: dV (DH cols), dK (DH cols), two S^T buffers and two dP^T buffers (STR cols
 // each; P^T and dS^T overwrite half of each elementwise warp's columns as bf16
-// pairs).  The score MMAs read K and V from the resident shared-memory tiles.
+// pairs), and where they fit K (K_IN_TMEM) and V (V_IN_TMEM) as packed bf16 pairs.
+// The score MMAs read K and V from TMEM when they are there, else from the resident
+// shared-memory tiles.
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fa2_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
