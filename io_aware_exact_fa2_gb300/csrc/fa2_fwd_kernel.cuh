@@ -71,6 +71,10 @@ struct FwdParams {
     int BH;                     // B * H
     int n_qgroups;              // ceil(Lq / (NQ * 128))
     int n_units;                // n_qgroups * BH
+    // causal: heads per group (BH: one group).  The heads are taken in groups whose K
+    // and V fit in L2 together, each group's units heaviest first and dealt out in a
+    // snake of its own, so that the units in flight re-read K/V prefixes from L2.
+    int head_group;
     int causal;
     // causal sliding window: query i sees keys i - window <= j <= i (-1: none)
     int window;
@@ -259,19 +263,49 @@ __device__ __forceinline__ int kv_tiles_for(int q0, int Lq, int Lk, int causal, 
 // The work unit a CTA handles at its i-th step, or -1 when it has no more.
 // Units are numbered heaviest first for causal (query groups from the bottom
 // of the score matrix up) and dealt to the CTAs in a snake, so a CTA that got
-// a heavy unit in one round gets a light one in the next.
-__device__ __forceinline__ int unit_at(int i, int n_units, int causal)
+// a heavy unit in one round gets a light one in the next.  GRP (causal passes whose
+// heads are taken in groups, head_group < BH): the units are numbered group of heads
+// by group of heads, and each group starts its snake at the first CTA again (the
+// direction alternating on from the previous group's last round), so every group is
+// balanced on its own.  GRP is a separate instantiation: the grouped form's loop,
+// inlined where it is never used, cost the other passes' step loops.
+template <bool GRP>
+__device__ __forceinline__ int unit_at(int i, const FwdParams &p)
 {
     const int g = static_cast<int>(gridDim.x);
     const int k = static_cast<int>(blockIdx.x);
-    const int idx = i * g + ((causal && (i & 1)) ? (g - 1 - k) : k);
-    return idx < n_units ? idx : -1;
+    if constexpr (GRP) {
+        int base = 0, rounds = 0;
+        for (int g0 = 0; g0 < p.BH; g0 += p.head_group) {
+            const int n = min(p.head_group, p.BH - g0) * p.n_qgroups;   // this group's units
+            const int full = n / g, rem = n % g;
+            // the partial last round reaches this CTA only if its snake position is below rem
+            const int pos_last = ((rounds + full) & 1) ? g - 1 - k : k;
+            const int mine = full + (rem > 0 && pos_last < rem ? 1 : 0);
+            if (i < mine)
+                return base + i * g + (((rounds + i) & 1) ? g - 1 - k : k);
+            i -= mine;
+            base += n;
+            rounds += full + (rem > 0 ? 1 : 0);
+        }
+        return -1;
+    } else {
+        const int idx = i * g + ((p.causal && (i & 1)) ? (g - 1 - k) : k);
+        return idx < p.n_units ? idx : -1;
+    }
 }
 
 // unit -> (query group, batch*head)
+template <bool GRP>
 __device__ __forceinline__ void decode_unit(int idx, const FwdParams &p, int &qg, int &bh)
 {
-    if (p.causal) {
+    if constexpr (GRP) {
+        const int per_group = p.head_group * p.n_qgroups;
+        const int gi = idx / per_group, r = idx - gi * per_group;
+        const int g0 = gi * p.head_group, gsize = min(p.head_group, p.BH - g0);
+        qg = p.n_qgroups - 1 - r / gsize;
+        bh = g0 + r % gsize;
+    } else if (p.causal) {
         qg = p.n_qgroups - 1 - idx / p.BH;
         bh = idx % p.BH;
     } else {
@@ -306,17 +340,18 @@ __device__ __forceinline__ int cta_of(int x, const SplitRanges &r)
     return lo;
 }
 
+template <bool GRP>
 __device__ __forceinline__ bool segment_at(int i, const FwdParams &p, const SplitRanges &r, Segment &sg)
 {
     if (!p.split) {
-        const int u = unit_at(i, p.n_units, p.causal);
+        const int u = unit_at<GRP>(i, p);
         if (u < 0)
             return false;
         sg.unit = u;
         sg.kv_lo = 0;
         if (p.window >= 0) {   // the unit's first K/V tile holding a key its first row may see
             int qg, bh;
-            decode_unit(u, p, qg, bh);
+            decode_unit<GRP>(u, p, qg, bh);
             sg.kv_lo = max(0, qg * p.unit_rows - p.window) / p.kv_rows;
         }
         sg.kv_hi = 0x7fffffff;
@@ -354,7 +389,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *er
     return __all_sync(0xffffffffu, ok);
 }
 
-template <class C>
+template <class C, bool GRP = false>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -428,10 +463,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             bool ok = true;
             for (int i = 0; ok; ++i) {
                 Segment sg;
-                if (!segment_at(i, p, ranges, sg))
+                if (!segment_at<GRP>(i, p, ranges, sg))
                     break;
                 int qg, bh;
-                decode_unit(sg.unit, p, qg, bh);
+                decode_unit<GRP>(sg.unit, p, qg, bh);
                 const int q0 = qg * (C::NQ * C::BM);
                 int n_max = 0;
 #pragma unroll
@@ -515,10 +550,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
             for (int i = 0; ok; ++i) {
                 Segment sg;
-                if (!segment_at(i, p, ranges, sg))
+                if (!segment_at<GRP>(i, p, ranges, sg))
                     break;
                 int qg, bh;
-                decode_unit(sg.unit, p, qg, bh);
+                decode_unit<GRP>(sg.unit, p, qg, bh);
                 const int q0 = qg * (C::NQ * C::BM);
                 int n_t[C::NQ];
                 int n_max = 0;
@@ -735,10 +770,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
         for (int i = 0; ok; ++i) {
             Segment sg;
-            if (!segment_at(i, p, ranges, sg))
+            if (!segment_at<GRP>(i, p, ranges, sg))
                 break;
             int qg, bh;
-            decode_unit(sg.unit, p, qg, bh);
+            decode_unit<GRP>(sg.unit, p, qg, bh);
             const int q0_t = qg * (C::NQ * C::BM) + t * C::BM;
             const int grow = q0_t + row;             // query index
             // score multiplier in log2 units (e4m3: the head's Q and K descales folded in)
@@ -997,7 +1032,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 // the next segment's Q goes into TMEM now, so its first S MMAs run during
                 // this epilogue
                 Segment next;
-                if (segment_at(i + 1, p, ranges, next) && !(ok = copy_q()))
+                if (segment_at<GRP>(i + 1, p, ranges, next) && !(ok = copy_q()))
                     break;
             }
 

@@ -157,6 +157,10 @@ inline bool encode_bhld_strided(EncodeTiledFn encode, CUtensorMap *m, const void
     return r == CUDA_SUCCESS;
 }
 
+#ifndef FA2_FWD_GROUP_MB
+#define FA2_FWD_GROUP_MB 96
+#endif
+
 template <class C>
 fa2_status launch_fwd(const LaunchArgs &a)
 {
@@ -184,6 +188,19 @@ fa2_status launch_fwd(const LaunchArgs &a)
     p.BH = BH;
     p.n_qgroups = (a.Lq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
     p.causal = a.causal ? 1 : 0;
+    // Causal passes whose K and V exceed FA2_FWD_GROUP_MB take the heads in that many
+    // evenly sized groups (each group's K and V fit in L2 beside the other traffic):
+    // all heads at once would stream every head's K/V prefixes in from DRAM again for
+    // each of its heaviest-first units.
+    p.head_group = BH;
+    if (a.causal) {
+        const long long per_head = 2ll * a.Lk * C::D * C::EB;   // K and V bytes of one head
+        const long long budget = static_cast<long long>(FA2_FWD_GROUP_MB) << 20;
+        if (budget > 0 && per_head * BH > budget) {
+            const long long groups = (per_head * BH + budget - 1) / budget;
+            p.head_group = static_cast<int>((BH + groups - 1) / groups);
+        }
+    }
     p.window = a.window;
     p.unit_rows = C::NQ * C::BM;
     p.kv_rows = C::BN;
@@ -215,18 +232,26 @@ fa2_status launch_fwd(const LaunchArgs &a)
         p.part_o = reinterpret_cast<float *>(base + w.part_o);
     }
 
-    // opt in to more than 48 KB of dynamic shared memory, once per device
+    // opt in to more than 48 KB of dynamic shared memory, once per device (both
+    // instantiations: whole units in one snake, and causal head groups)
     static std::atomic<unsigned long long> configured{0};
     const unsigned long long bit = (a.device >= 0 && a.device < 64) ? (1ull << a.device) : 0ull;
     if (!bit || !(configured.load() & bit)) {
-        if (cudaFuncSetAttribute(fa2_fwd_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(fa2_fwd_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fa2_fwd_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM_BYTES) != cudaSuccess) {
             (void)cudaGetLastError();
             return FA2_ERR_CUDA;
         }
         configured.fetch_or(bit);
     }
-    fa2_fwd_kernel<C><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, to, p, ranges);
+    if (p.causal && p.head_group < BH)
+        fa2_fwd_kernel<C, true><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(
+            tq, tk, tv, to, p, ranges);
+    else
+        fa2_fwd_kernel<C, false><<<static_cast<unsigned>(grid), C::NUM_THREADS, C::SMEM_BYTES, a.stream>>>(
+            tq, tk, tv, to, p, ranges);
     return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 

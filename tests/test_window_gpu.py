@@ -96,6 +96,21 @@ def test_wide_window_is_plain_causal_bit_for_bit():
     assert torch.equal(o_w, o_c) and torch.equal(l_w, l_c)
 
 
+def test_window_with_causal_head_groups():
+    """B1 H32 L16384 D128 with a 1024-key window: the heads' K and V (256 MB) exceed the L2
+    budget, so the pass takes its heads in groups (each with its own heaviest-first snake);
+    sampled rows (tile edges of the first and last head + random) against the oracle."""
+    B, H, L, D, w = 1, 32, 16384, 128, 1024
+    q, k, v = make_qkv(B, H, L, L, D, seed_base=9350)
+    o, lse = run_window(q, k, v, w, scale_of(D))
+    rows = sample_rows(B, H, L, n_random=384, seed=9351)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, True, scale_of(D), rows, window=w)
+    idx = torch.from_numpy(rows)
+    n_flat = compare(o.reshape(-1, D)[idx], lse.reshape(-1)[idx], o_ref, lse_ref, v, w, L, rows=rows)
+    assert n_flat >= 0.9 * len(rows)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
 def test_window_at_the_forward_bench_size():
     """B2 H16 L4096 D128 with a 1024-key window: sampled rows (tile edges + random)."""
     B, H, L, D, w = 2, 16, 4096, 128, 1024
