@@ -194,7 +194,12 @@ fa2_status launch_fwd(const LaunchArgs &a)
     // each of its heaviest-first units.
     p.head_group = BH;
     if (a.causal) {
-        const long long per_head = 2ll * a.Lk * C::D * C::EB;   // K and V bytes of one head
+        // K and V rows a head's units read: all of them, or under a sliding window the
+        // band (window + a unit's rows + one K/V tile), the same for every unit
+        long long rows = a.Lk;
+        if (a.window >= 0 && a.window + static_cast<long long>(C::NQ * C::BM + C::BN) < rows)
+            rows = a.window + static_cast<long long>(C::NQ * C::BM + C::BN);
+        const long long per_head = 2ll * rows * C::D * C::EB;   // K and V bytes of one head
         const long long budget = static_cast<long long>(FA2_FWD_GROUP_MB) << 20;
         if (budget > 0 && per_head * BH > budget) {
             const long long groups = (per_head * BH + budget - 1) / budget;

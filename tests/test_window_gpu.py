@@ -97,10 +97,11 @@ def test_wide_window_is_plain_causal_bit_for_bit():
 
 
 def test_window_with_causal_head_groups():
-    """B1 H32 L16384 D128 with a 1024-key window: the heads' K and V (256 MB) exceed the L2
-    budget, so the pass takes its heads in groups (each with its own heaviest-first snake);
-    sampled rows (tile edges of the first and last head + random) against the oracle."""
-    B, H, L, D, w = 1, 32, 16384, 128, 1024
+    """B1 H32 L16384 D128 with an 8192-key window: the K and V rows the heads' units read
+    (each head's band, 140 MB over all heads) exceed the L2 budget, so the pass takes its
+    heads in groups (each with its own heaviest-first snake); sampled rows (tile edges of
+    the first and last head + random) against the oracle."""
+    B, H, L, D, w = 1, 32, 16384, 128, 8192
     q, k, v = make_qkv(B, H, L, L, D, seed_base=9350)
     o, lse = run_window(q, k, v, w, scale_of(D))
     rows = sample_rows(B, H, L, n_random=384, seed=9351)
